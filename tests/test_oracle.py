@@ -1,0 +1,263 @@
+"""Pins for the fp64 oracle: each check ties it to something other than itself.
+
+CPU only. The checks and what each would catch:
+
+* full-vocabulary KL against ``scipy.stats.entropy`` (a library KL): a wrong
+  sign, a dropped lse, a transposed projection;
+* student equal to teacher, full and truncated: zero loss, and a gradient that
+  is either zero (K = V) or the closed form (S - 1) q on the cached ids and S q
+  elsewhere (K < V);
+* the log-sum inequality loss_n >= S_n log(S_n / Q_n), with equality when the
+  teacher is proportional to the student on its ids;
+* gradient rows summing to zero, hence vocabulary-summed dW equal to zero;
+* central finite differences of the loss against dH and dW;
+* the "Dense KL" variant built from ``torch.nn.functional.kl_div`` + autograd;
+* chunk invariance ("mathematically equivalent" variants);
+* -inf cache entries and repeated ids, as reductions to other problems;
+* a stored fixture written by ``tests/golden/make_golden.py`` from the oracle.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import scipy.stats
+
+from oracle import fckl_oracle as orc
+from oracle.dense_kl import dense_kl
+import synthetic
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _problem(N, d, V, K, seed=0, dtype="f32"):
+    return synthetic.make_inputs(N, d, V, K, dtype=dtype, seed=seed)
+
+
+def test_generator_recipe():
+    x = _problem(32, 16, 500, 20, seed=3)
+    idx, logp = x["idx"], x["logp"]
+    assert idx.dtype == np.int32 and logp.dtype == np.float32
+    assert all(len(set(r)) == 20 for r in idx.tolist())
+    assert idx.min() >= 0 and idx.max() < 500
+    assert np.all(np.diff(logp, axis=1) <= 0)
+    S = np.exp(logp.astype(np.float64)).sum(1)
+    assert np.all(S > 0.85 - 1e-6) and np.all(S < 0.99 + 1e-6)
+    # not sorted by id: draw order is kept
+    assert not np.all(np.diff(idx, axis=1) > 0)
+    # bf16 rounding leaves values representable in bf16
+    y = _problem(4, 16, 64, 4, dtype="bf16")
+    bits = y["W"].view(np.uint32)
+    assert np.all(bits & 0xFFFF == 0)
+
+
+def test_full_vocab_kl_matches_library():
+    rng = np.random.default_rng(1)
+    N, d, V = 6, 12, 40
+    H = rng.standard_normal((N, d))
+    W = rng.standard_normal((V, d)) / np.sqrt(d)
+    t = rng.standard_normal((N, V)) * 2.0
+    p_dense = scipy.special.softmax(t, axis=1)
+    idx = np.stack([rng.permutation(V) for _ in range(N)])
+    logp = np.log(np.take_along_axis(p_dense, idx, axis=1))
+    loss, lse, rl = orc.forward(H, W, idx, logp)
+    q = scipy.special.softmax(H @ W.T, axis=1)
+    want = np.array([scipy.stats.entropy(p_dense[n], q[n]) for n in range(N)])
+    np.testing.assert_allclose(rl, want, rtol=1e-12, atol=1e-14)
+    assert loss == pytest.approx(want.sum(), rel=1e-12)
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(H @ W.T, axis=1), rtol=1e-14)
+
+
+def test_student_equals_teacher_full_vocab():
+    rng = np.random.default_rng(2)
+    N, d, V = 5, 10, 30
+    H = rng.standard_normal((N, d))
+    W = rng.standard_normal((V, d))
+    logq = scipy.special.log_softmax(H @ W.T, axis=1)
+    idx = np.stack([rng.permutation(V) for _ in range(N)])
+    logp = np.take_along_axis(logq, idx, axis=1)
+    loss, _, rl = orc.forward(H, W, idx, logp)
+    assert abs(loss) < 1e-12
+    dH, dW = orc.backward(H, W, idx, logp)
+    assert np.abs(dH).max() < 1e-12 and np.abs(dW).max() < 1e-12
+
+
+def test_student_equals_teacher_truncated():
+    rng = np.random.default_rng(3)
+    N, d, V, K = 4, 9, 50, 7
+    H = rng.standard_normal((N, d))
+    W = rng.standard_normal((V, d))
+    z = H @ W.T
+    logq = scipy.special.log_softmax(z, axis=1)
+    idx = np.argsort(-z, axis=1)[:, :K]
+    logp = np.take_along_axis(logq, idx, axis=1)
+    loss, lse, rl = orc.forward(H, W, idx, logp)
+    assert np.abs(rl).max() < 1e-13
+    # K < V: S < 1, and the gradient is (S-1) q on the cached ids, S q off them.
+    q = np.exp(logq)
+    S = np.take_along_axis(q, idx, axis=1).sum(1)
+    want = S[:, None] * q
+    for n in range(N):
+        want[n, idx[n]] = (S[n] - 1.0) * q[n, idx[n]]
+    G = orc.logit_grad(z, lse, idx, logp)
+    np.testing.assert_allclose(G, want, rtol=1e-11, atol=1e-15)
+    dH, dW = orc.backward(H, W, idx, logp)
+    np.testing.assert_allclose(dH, want @ W, rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(dW, want.T @ H, rtol=1e-10, atol=1e-13)
+
+
+def test_log_sum_bound_and_equality():
+    x = _problem(48, 32, 700, 25, seed=4)
+    loss, lse, rl = orc.forward(x["H"], x["W"], x["idx"], x["logp"])
+    z = orc.logits(x["H"], x["W"])
+    q = scipy.special.softmax(z, axis=1)
+    Q = np.take_along_axis(q, x["idx"].astype(np.int64), axis=1).sum(1)
+    S = np.exp(x["logp"].astype(np.float64)).sum(1)
+    bound = S * np.log(S / Q)
+    assert np.all(rl >= bound - 1e-12)
+    assert np.any(rl > bound + 1e-3)
+    # equality when the teacher is proportional to the student on its ids
+    qk = np.take_along_axis(q, x["idx"].astype(np.int64), axis=1)
+    logp_eq = np.log(S[:, None] * qk / Q[:, None])
+    _, _, rl_eq = orc.forward(x["H"], x["W"], x["idx"], logp_eq)
+    np.testing.assert_allclose(rl_eq, bound, rtol=1e-10, atol=1e-12)
+
+
+def test_gradient_rows_and_dW_sum_to_zero():
+    x = _problem(40, 24, 300, 10, seed=5)
+    z = orc.logits(x["H"], x["W"])
+    lse = orc.log_partition(z)
+    G = orc.logit_grad(z, lse, x["idx"], x["logp"])
+    assert np.abs(G.sum(1)).max() < 1e-14 * 300
+    _, dW = orc.backward(x["H"], x["W"], x["idx"], x["logp"])
+    assert np.abs(dW.sum(0)).max() < 1e-12 * np.abs(dW).max() * 300
+
+
+def test_finite_differences():
+    rng = np.random.default_rng(6)
+    N, d, V, K = 4, 8, 32, 5
+    H = rng.standard_normal((N, d))
+    W = rng.standard_normal((V, d)) / np.sqrt(d)
+    idx, logp = synthetic.teacher_cache(N, V, K, seed=7)
+    scale = 1.7
+    dH, dW = orc.backward(H, W, idx, logp, grad_scale=scale)
+    h = 1e-6
+
+    def f(Hx, Wx):
+        return scale * orc.forward(Hx, Wx, idx, logp)[0]
+
+    for _ in range(10):
+        i, j = rng.integers(N), rng.integers(d)
+        Hp, Hm = H.copy(), H.copy()
+        Hp[i, j] += h
+        Hm[i, j] -= h
+        fd = (f(Hp, W) - f(Hm, W)) / (2 * h)
+        assert fd == pytest.approx(dH[i, j], rel=1e-6, abs=1e-8)
+        v, j = rng.integers(V), rng.integers(d)
+        Wp, Wm = W.copy(), W.copy()
+        Wp[v, j] += h
+        Wm[v, j] -= h
+        fd = (f(H, Wp) - f(H, Wm)) / (2 * h)
+        assert fd == pytest.approx(dW[v, j], rel=1e-6, abs=1e-8)
+
+
+def test_dense_kl_variant_agrees():
+    x = _problem(64, 256, 4096, 16, seed=0)
+    loss, lse, dH, dW = orc.forward_backward(x["H"], x["W"], x["idx"], x["logp"], grad_scale=0.5)
+    dl, dHd, dWd = dense_kl(x["H"], x["W"], x["idx"], x["logp"], grad_scale=0.5)
+    assert loss == pytest.approx(dl, rel=1e-12)
+    assert np.abs(dH - dHd).max() <= 1e-10 * np.abs(dHd).max()
+    assert np.abs(dW - dWd).max() <= 1e-10 * np.abs(dWd).max()
+
+
+def test_chunk_invariance():
+    x = _problem(23, 16, 200, 9, seed=8)
+    ref = orc.forward_backward(x["H"], x["W"], x["idx"], x["logp"], chunk=None)
+    for chunk in (1, 7, 16, 23, 64):
+        got = orc.forward_backward(x["H"], x["W"], x["idx"], x["logp"], chunk=chunk)
+        assert got[0] == pytest.approx(ref[0], rel=1e-12)
+        for a, b in zip(got[1:], ref[1:]):
+            np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-14)
+
+
+def test_neg_inf_slots_drop_out():
+    x = _problem(12, 16, 128, 6, seed=9)
+    logp = x["logp"].copy()
+    logp[:, -1] = -np.inf
+    full = orc.forward_backward(x["H"], x["W"], x["idx"], logp)
+    cut = orc.forward_backward(x["H"], x["W"], x["idx"][:, :-1], x["logp"][:, :-1])
+    assert np.isfinite(full[0])
+    assert full[0] == pytest.approx(cut[0], rel=1e-13)
+    for a, b in zip(full[1:], cut[1:]):
+        np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-15)
+
+
+def test_repeated_ids_split_slot():
+    x = _problem(10, 16, 128, 6, seed=10)
+    idx, logp = x["idx"], x["logp"].astype(np.float64)
+    # slot 0 split into two slots with the same id and half the probability each
+    idx2 = np.concatenate([idx[:, :1], idx], axis=1)
+    logp2 = np.concatenate([logp[:, :1] - np.log(2.0), logp[:, :1] - np.log(2.0), logp[:, 1:]], axis=1)
+    base = orc.forward_backward(x["H"], x["W"], idx, logp)
+    split = orc.forward_backward(x["H"], x["W"], idx2, logp2)
+    shift = -(np.exp(logp[:, 0]) * np.log(2.0)).sum()
+    assert split[0] == pytest.approx(base[0] + shift, rel=1e-12)
+    for a, b in zip(split[1:], base[1:]):
+        np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-15)
+    # gradients equal the dense variant's, which merges the repeated slots
+    _, dHd, dWd = dense_kl(x["H"], x["W"], idx2, logp2)
+    np.testing.assert_allclose(split[2], dHd, rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(split[3], dWd, rtol=1e-10, atol=1e-13)
+
+
+def test_grad_scale_is_linear():
+    x = _problem(9, 16, 100, 5, seed=11)
+    a = orc.backward(x["H"], x["W"], x["idx"], x["logp"], grad_scale=1.0)
+    b = orc.backward(x["H"], x["W"], x["idx"], x["logp"], grad_scale=-2.5)
+    np.testing.assert_allclose(b[0], -2.5 * a[0], rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(b[1], -2.5 * a[1], rtol=1e-12, atol=1e-15)
+
+
+def test_rows_match_full_pass():
+    x = _problem(30, 32, 256, 8, seed=12)
+    loss, lse, rl = orc.forward(x["H"], x["W"], x["idx"], x["logp"])
+    dH, _ = orc.backward(x["H"], x["W"], x["idx"], x["logp"], grad_scale=0.25)
+    which = [0, 7, 29]
+    l2, r2, h2 = orc.rows(x["H"], x["W"], x["idx"], x["logp"], which, grad_scale=0.25)
+    np.testing.assert_allclose(l2, lse[which], rtol=1e-14)
+    np.testing.assert_allclose(r2, rl[which], rtol=1e-13)
+    np.testing.assert_allclose(h2, dH[which], rtol=1e-12, atol=1e-15)
+
+
+def test_bad_index_rejected():
+    x = _problem(4, 8, 32, 3, seed=13)
+    idx = x["idx"].copy()
+    idx[1, 2] = 32
+    with pytest.raises(IndexError):
+        orc.forward(x["H"], x["W"], idx, x["logp"])
+
+
+def test_lse_statistics_sanity():
+    """Not a pin: with z ~ N(0, 1), E[exp z] = e^(1/2), so lse is near ln V + 1/2."""
+    x = _problem(64, 256, 4096, 16, seed=0)
+    _, lse, _ = orc.forward(x["H"], x["W"], x["idx"], x["logp"])
+    assert abs(lse.mean() - (np.log(4096) + 0.5)) < 0.05
+
+
+def test_golden_fixture():
+    """Values stored by tests/golden/make_golden.py from the oracle itself: catch
+    unintended changes of the oracle or of the generators on another machine."""
+    with open(os.path.join(GOLDEN, "tiny_oracle.json")) as f:
+        g = json.load(f)
+    w = synthetic.WORKLOADS[g["workload"]]
+    x = synthetic.make_inputs(w.N, w.d, w.V, w.K, dtype=w.dtype, seed=g["seed"])
+    assert x["idx"][0, :8].tolist() == g["idx_row0"]
+    np.testing.assert_array_equal(x["logp"][0, :4], np.array(g["logp_row0"], np.float32))
+    np.testing.assert_array_equal(x["H"][0, :4], np.array(g["H_row0"], np.float32))
+    loss, lse, dH, dW = orc.forward_backward(x["H"], x["W"], x["idx"], x["logp"],
+                                             grad_scale=g["grad_scale"], chunk=w.chunk)
+    assert loss == pytest.approx(g["loss"], rel=1e-12)
+    np.testing.assert_allclose(lse[:8], g["lse_head"], rtol=1e-12)
+    np.testing.assert_allclose(dH[0, :8], g["dH_row0"], rtol=1e-10, atol=1e-14)
+    np.testing.assert_allclose(dW[x["idx"][0, 0], :8], g["dW_hit_row"], rtol=1e-10, atol=1e-14)
