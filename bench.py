@@ -1,0 +1,387 @@
+"""Benchmark of the fused, chunked top-K KL loss: forward + backward on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = fckl_forward + fckl_backward over the whole workload (all chunks), inputs
+resident in HBM. Prints one JSON line (rank 0). Under torchrun each rank runs its own
+replica of the workload (the loss has no exchange step on one GPU: replicas only) and
+the whole-job value is the positions of all ranks over the slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle, as it stands, on the host cores, on a
+bounded sample of positions of the same workload (the pages ship no runnable code).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic  # noqa: E402
+
+DEFAULT_WORKLOAD = "n32768_d3072_v128256"
+METRIC = "fused KL fwd+bwd positions/s & TFLOP/s (8NdV) vs BF16 roofline; peak GiB"
+UNIT = "positions/s"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_KERNELS = ("fwd_logits_lse", "bwd_logit_grad", "bwd_dH_gemm", "bwd_dW_gemm")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def sample_rows_oracle(w, x_rows, W_full, n_rows):
+    """One oracle forward+backward over the first n_rows positions (full V and d)."""
+    from oracle import fckl_oracle as orc
+    sl = slice(0, n_rows)
+    t0 = time.perf_counter()
+    loss, lse, _ = orc.forward(x_rows["H"][sl], W_full, x_rows["idx"][sl], x_rows["logp"][sl], w.chunk)
+    dH, dW = orc.backward(x_rows["H"][sl], W_full, x_rows["idx"][sl], x_rows["logp"][sl], 1.0, w.chunk)
+    return time.perf_counter() - t0
+
+
+def cpu_inputs(w, seed, n_rows):
+    """The first n_rows positions of the workload's inputs, and the full W (same recipe)."""
+    H = synthetic.hidden_states(n_rows, w.d, seed + 0)
+    W = synthetic.output_projection(w.V, w.d, seed + 1)
+    idx, logp = synthetic.teacher_cache(n_rows, w.V, w.K, seed + 2)
+    if w.dtype == "bf16":
+        H, W = synthetic.round_bf16(H), synthetic.round_bf16(W)
+    return {"H": H, "idx": idx, "logp": logp}, W
+
+
+def oracle_sample_size(w, target_s=15.0):
+    """Rows of a CPU sample taking roughly target_s seconds (cost is linear in rows)."""
+    per_row_flops = 8.0 * w.d * w.V
+    guess = int(target_s * 100e9 / per_row_flops)  # ~100 GFLOP/s fp64 BLAS as a first guess
+    return max(8, min(w.N, guess))
+
+
+def cpu_baseline(w, seed):
+    n = oracle_sample_size(w)
+    x, W = cpu_inputs(w, seed, n)
+    t = sample_rows_oracle(w, x, W, n)
+    return {"value": n / t, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+            "sample": f"fp64 oracle forward+backward on the first {n} of {w.N} positions "
+                      f"(full V={w.V}, d={w.d}, K={w.K}), {t:.1f} s; cost is linear in positions"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = synthetic.WORKLOADS[args.workload]
+    n = max(8, oracle_sample_size(w, target_s=6.0))
+    x, W = cpu_inputs(w, args.seed, n)
+    for _ in range(args.warmup):
+        sample_rows_oracle(w, x, W, min(n, 8))
+    times = [sample_rows_oracle(w, x, W, n) for _ in range(args.steps)]
+    t = sum(times)
+    value = n * args.steps / t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": config_of(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                             "sample": f"each step: fp64 oracle forward+backward on {n} of {w.N} positions "
+                                       f"(full V, d)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w):
+    return {"workload": w.name, "N": w.N, "d": w.d, "V": w.V, "K": w.K, "chunk": w.chunk,
+            "input_dtype": w.dtype, "parallelism": "replicas",
+            "l2": "inputs larger than L2 (W alone is %.0f MB)" % (w.V * w.d * 2 / 1e6)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as f:
+                d = json.load(f)
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK), "fallback"
+
+
+def peak_value(peaks, key):
+    for k, v in peaks.items():
+        if k == key and isinstance(v, (int, float)):
+            return float(v)
+    for k, v in peaks.items():
+        if key in k and isinstance(v, (int, float)):
+            return float(v)
+    return FALLBACK[key]
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    cdir = os.path.join(ROOT, "chunked_kl_loss_gb300", "csrc")
+    for name in sorted(os.listdir(cdir)):
+        with open(os.path.join(cdir, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m or not t or m.group(1) != kernel_source_hash():
+        return None
+    return float(t.group(1))
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_ours(args):
+    import torch
+    import chunked_kl_loss_gb300 as fckl
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    fckl.load()
+    w = synthetic.WORKLOADS[args.workload]
+    x = synthetic.make_inputs(w.N, w.d, w.V, w.K, dtype="f32", seed=args.seed + 1000 * rank)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    host = {
+        "H": torch.from_numpy(x["H"]).to(tdt).pin_memory(),
+        "W": torch.from_numpy(x["W"]).to(tdt).pin_memory(),
+        "idx": torch.from_numpy(x["idx"]).pin_memory(),
+        "logp": torch.from_numpy(x["logp"]).pin_memory(),
+    }
+    del x
+    torch.cuda.reset_peak_memory_stats(dev)
+    base_alloc = torch.cuda.memory_allocated(dev)
+    H, W, idx, logp = (host[k].to(dev) for k in ("H", "W", "idx", "logp"))
+    dt = fckl.BF16 if w.dtype == "bf16" else fckl.F32
+    ws = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, dt, dev)
+    dH = torch.empty_like(H)
+    dW = torch.empty(w.V, w.d, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        loss, lse = fckl.forward(H, W, idx, logp, w.chunk, ws=ws, stream=stream)
+        fckl.backward(H, W, idx, logp, lse, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW)
+        return loss
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    fckl.check(ws)
+    barrier()
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    fckl.profile_enable(True)
+    fckl.profile_read()
+    launches0 = fckl.launch_count()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        loss = step()
+    e1.record(stream)
+    barrier()
+    elapsed_ms = e0.elapsed_time(e1)
+    launches = fckl.launch_count() - launches0
+    prof = fckl.profile_read()
+    fckl.profile_enable(False)
+    clk = clocks.stop()
+    fckl.check(ws)
+    peak_bytes = torch.cuda.max_memory_allocated(dev) - base_alloc
+
+    t_max = elapsed_ms
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+
+    # end to end through the public API from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            Hd, Wd, idd, lpd = (host[k].to(dev, non_blocking=True) for k in ("H", "W", "idx", "logp"))
+            loss, lse = fckl.forward(Hd, Wd, idd, lpd, w.chunk, ws=ws, stream=stream)
+            fckl.backward(Hd, Wd, idd, lpd, lse, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW)
+            loss_host.copy_(loss, non_blocking=True)
+
+        e2e_step()
+        barrier()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        f1.record(stream)
+        barrier()
+        e2e_ms = f0.elapsed_time(f1)
+        if world > 1:
+            import torch.distributed as dist
+            tt = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        h2d = sum(host[k].numel() * host[k].element_size() for k in host)
+        e2e = {"value": world * w.N * args.steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": 4, "ms_per_step": e2e_ms / args.steps}
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    ms_step = t_max / args.steps
+    value = world * w.N * args.steps / (t_max / 1e3)
+    tflops = w.flops() / (ms_step / 1e3) / 1e12
+    peaks, peak_src = measured_peaks()
+    peak_sus = peak_value(peaks, "bf16_tflops_sustained")
+    # dominant kernel: largest share of the measured launch time
+    kname, (kms, kn) = max(prof.items(), key=lambda kv: kv[1][0])
+    roof = None
+    if kname in GEMM_KERNELS and kn > 0:
+        flops_per_launch = 2.0 * w.N * w.d * w.V * args.steps / kn
+        achieved = flops_per_launch / (kms / kn / 1e3) / 1e12
+        traffic = profile_traffic(kname, w.name)
+        roof = {"kernel": kname, "bound": "tensor", "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
+                "frac": achieved / peak_sus, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step)",
+                "flops_per_launch": flops_per_launch, "avg_launch_ms": kms / kn}
+    shares = {k: round(v[0] / max(1e-9, sum(u[0] for u in prof.values())), 4) for k, v in prof.items() if v[1]}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generators; no dataset)",
+        "config": config_of(w),
+        "tflops": tflops, "tflops_frac_of_peak": tflops / peak_sus,
+        "peak_gib": peak_bytes / 2**30,
+        "gpu_launches": launches,
+        "roofline": roof,
+        "kernel_shares": shares,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, args.seed)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,225 @@
+"""Fused, chunked top-K KL distillation loss on GB300: Python binding of ``include/fckl.h``.
+
+Argument marshalling only. Every step of the loss and its gradients runs in the CUDA
+library ``_build/libfckl.so``; PyTorch supplies device memory and the stream. There is
+no CPU fallback: if the library is missing, ``load()`` raises.
+
+Typical use (tensors on the current CUDA device)::
+
+    import chunked_kl_loss_gb300 as fckl
+    loss, lse = fckl.forward(H, W, idx, logp, chunk=2048)
+    dH, dW = fckl.backward(H, W, idx, logp, lse, chunk=2048)
+    fckl.check()            # raises on a device-detected error (bad teacher id, timeout)
+
+``H [N, d]`` and ``W [V, d]`` are bf16 or fp32, ``idx [N, K]`` int32 teacher token ids,
+``logp [N, K]`` fp32 teacher log-probabilities (not renormalised). The loss is a sum over
+positions; ``grad_scale`` carries an upstream derivative (e.g. ``1/N`` for a mean).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = ["LIB_PATH", "FcklError", "load", "workspace_bytes", "Workspace", "forward", "backward",
+           "forward_backward", "check", "launch_count", "profile_enable", "profile_read",
+           "kernel_names", "OK", "ERR_ARG", "ERR_INDEX", "ERR_CUDA", "ERR_TIMEOUT",
+           "ERR_WORKSPACE", "ERR_UNSUPPORTED"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfckl.so")
+
+OK, ERR_ARG, ERR_INDEX, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_UNSUPPORTED = range(7)
+BF16, F32 = 0, 1
+
+_lib = None
+
+
+class FcklError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        msg = load().fckl_status_string(status).decode()
+        extra = load().fckl_last_error().decode() if status == ERR_CUDA else ""
+        super().__init__(f"{where}: {msg}" + (f" ({extra})" if extra else ""))
+
+
+def load():
+    """Loads the CUDA library (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                           "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+    lib = ctypes.CDLL(LIB_PATH)
+    c = ctypes
+    vp, i64, i32, sz, f32 = c.c_void_p, c.c_int64, c.c_int, c.c_size_t, c.c_float
+    lib.fckl_workspace_bytes.restype = sz
+    lib.fckl_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
+    lib.fckl_forward.restype = i32
+    lib.fckl_forward.argtypes = [vp, vp, i32, vp, vp, i64, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+    lib.fckl_backward.restype = i32
+    lib.fckl_backward.argtypes = [vp, vp, i32, vp, vp, vp, i64, i32, i32, i32, i32, f32, vp, vp, vp, sz, vp]
+    lib.fckl_check.restype = i32
+    lib.fckl_check.argtypes = [vp, vp]
+    lib.fckl_status_string.restype = c.c_char_p
+    lib.fckl_status_string.argtypes = [i32]
+    lib.fckl_last_error.restype = c.c_char_p
+    lib.fckl_last_error.argtypes = []
+    lib.fckl_launch_count.restype = i64
+    lib.fckl_launch_count.argtypes = []
+    lib.fckl_profile_enable.restype = i32
+    lib.fckl_profile_enable.argtypes = [i32]
+    lib.fckl_profile_read.restype = i32
+    lib.fckl_profile_read.argtypes = [c.POINTER(c.c_double), c.POINTER(c.c_int64), i32]
+    lib.fckl_kernel_name.restype = c.c_char_p
+    lib.fckl_kernel_name.argtypes = [i32]
+    _lib = lib
+    return lib
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"H and W must be bfloat16 or float32, got {t.dtype}")
+
+
+def _stream_ptr(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def workspace_bytes(N: int, d: int, V: int, K: int, chunk: int, dtype: int = BF16) -> int:
+    return int(load().fckl_workspace_bytes(N, d, V, K, chunk, dtype))
+
+
+class Workspace:
+    """A device workspace sized for one problem shape (a torch uint8 tensor)."""
+
+    def __init__(self, N, d, V, K, chunk, dtype=BF16, device=None):
+        import torch
+        n = workspace_bytes(N, d, V, K, chunk, dtype)
+        if n == 0:
+            raise FcklError(ERR_UNSUPPORTED, "workspace_bytes")
+        self.nbytes = n
+        self.tensor = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.tensor.data_ptr())
+
+
+_last_ws = None
+
+
+def _shape(H, W, idx, logp):
+    N, d = H.shape
+    V = W.shape[0]
+    K = idx.shape[1]
+    if W.shape[1] != d or idx.shape[0] != N or tuple(logp.shape) != tuple(idx.shape):
+        raise ValueError("expected H [N,d], W [V,d], idx [N,K], logp [N,K]")
+    if H.dtype != W.dtype:
+        raise TypeError("H and W must share a dtype")
+    for t in (H, W, idx, logp):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    return N, d, V, K
+
+
+def _ws_for(ws, N, d, V, K, chunk, dt, device):
+    global _last_ws
+    if ws is None:
+        ws = Workspace(N, d, V, K, chunk, dt, device)
+    _last_ws = ws
+    return ws
+
+
+def forward(H, W, idx, logp, chunk, ws=None, stream=None, row_loss=False):
+    """Returns (loss [1] fp32, lse [N] fp32) or, with ``row_loss=True``, also the
+    per-position losses [N]."""
+    import torch
+    N, d, V, K = _shape(H, W, idx, logp)
+    dt = _dtype_code(H)
+    ws = _ws_for(ws, N, d, V, K, chunk, dt, H.device)
+    loss = torch.empty(1, dtype=torch.float32, device=H.device)
+    lse = torch.empty(N, dtype=torch.float32, device=H.device)
+    rl = torch.empty(N, dtype=torch.float32, device=H.device) if row_loss else None
+    st = load().fckl_forward(_ptr(H), _ptr(W), dt, _ptr(idx), _ptr(logp), N, d, V, K, chunk,
+                             _ptr(loss), _ptr(lse), _ptr(rl), ws.ptr, ws.nbytes, _stream_ptr(stream))
+    if st != OK:
+        raise FcklError(st, "fckl_forward")
+    return (loss, lse, rl) if row_loss else (loss, lse)
+
+
+def backward(H, W, idx, logp, lse, chunk, grad_scale=1.0, ws=None, stream=None, dH=None, dW=None):
+    """Returns (dH [N,d] in H's dtype, dW [V,d] fp32)."""
+    import torch
+    N, d, V, K = _shape(H, W, idx, logp)
+    dt = _dtype_code(H)
+    ws = _ws_for(ws, N, d, V, K, chunk, dt, H.device)
+    if dH is None:
+        dH = torch.empty_like(H)
+    if dW is None:
+        dW = torch.empty(V, d, dtype=torch.float32, device=H.device)
+    st = load().fckl_backward(_ptr(H), _ptr(W), dt, _ptr(idx), _ptr(logp), _ptr(lse), N, d, V, K, chunk,
+                              float(grad_scale), _ptr(dH), _ptr(dW), ws.ptr, ws.nbytes, _stream_ptr(stream))
+    if st != OK:
+        raise FcklError(st, "fckl_backward")
+    return dH, dW
+
+
+def forward_backward(H, W, idx, logp, chunk, grad_scale=1.0, ws=None, stream=None):
+    """(loss, lse, dH, dW) from one forward and one backward call sharing a workspace."""
+    N, d, V, K = _shape(H, W, idx, logp)
+    ws = _ws_for(ws, N, d, V, K, chunk, _dtype_code(H), H.device)
+    loss, lse = forward(H, W, idx, logp, chunk, ws=ws, stream=stream)
+    dH, dW = backward(H, W, idx, logp, lse, chunk, grad_scale=grad_scale, ws=ws, stream=stream)
+    return loss, lse, dH, dW
+
+
+def check(ws=None, stream=None, raise_on_error=True) -> int:
+    """Synchronises and reads the device status word of ``ws`` (default: the workspace
+    of the last call); raises FcklError on a device-detected error."""
+    ws = ws if ws is not None else _last_ws
+    if ws is None:
+        return OK
+    st = load().fckl_check(ws.ptr, _stream_ptr(stream))
+    if st != OK and raise_on_error:
+        raise FcklError(st, "device status")
+    return st
+
+
+def launch_count() -> int:
+    return int(load().fckl_launch_count())
+
+
+def profile_enable(on: bool = True) -> None:
+    load().fckl_profile_enable(1 if on else 0)
+
+
+def kernel_names():
+    lib = load()
+    out = []
+    while True:
+        n = lib.fckl_kernel_name(len(out))
+        if n is None:
+            return out
+        out.append(n.decode())
+
+
+def profile_read():
+    """{kernel name: (total ms, launches)} since the last read."""
+    names = kernel_names()
+    ms = (ctypes.c_double * len(names))()
+    ln = (ctypes.c_int64 * len(names))()
+    st = load().fckl_profile_read(ms, ln, len(names))
+    if st != OK:
+        raise FcklError(st, "fckl_profile_read")
+    return {n: (ms[i], int(ln[i])) for i, n in enumerate(names)}

@@ -1,0 +1,603 @@
+// Host side of the fused, chunked top-K KL loss: argument checks, workspace carving,
+// tensor-map encoding, the chunk loop and the kernel launches behind include/fckl.h.
+//
+// Forward, per chunk of positions ("Fused, chunked KL loss": project the chunk, fold it
+// into the running loss, drop it):
+//   preprocess -> fwd_logits_lse (tcgen05, online max/sum-exp + top-K gather) -> combine
+// then one fixed-order sum of the per-position losses.
+// Backward, per chunk (the chunk's logits are recomputed):
+//   preprocess -> bwd_logit_grad (tcgen05, G to a bf16 chunk x V slab)
+//              -> dH = G W (tcgen05, split over V, fp32 partials) -> dH reduce
+//              -> dW (+)= G^T H_chunk (tcgen05, TMA store on the first chunk, TMA
+//                 reduce-add afterwards)
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/fckl.h"
+#include "simt.cuh"
+#include "tc_gemm.cuh"
+
+namespace fckl {
+namespace {
+
+enum Kind {
+  KIND_PREPROCESS = 0,
+  KIND_FWD_LOGITS,
+  KIND_FWD_COMBINE,
+  KIND_LOSS_REDUCE,
+  KIND_BWD_GRAD,
+  KIND_BWD_DH,
+  KIND_BWD_DH_REDUCE,
+  KIND_BWD_DW,
+  KIND_CVT,
+  KIND_COUNT
+};
+const char* const kKindNames[KIND_COUNT] = {"preprocess",     "fwd_logits_lse", "fwd_combine",
+                                            "loss_reduce",    "bwd_logit_grad", "bwd_dH_gemm",
+                                            "bwd_dH_reduce",  "bwd_dW_gemm",    "cvt_bf16"};
+
+// ------------------------------------------------------------------ process state
+std::mutex g_mu;
+char g_last_error[512] = "";
+long long g_launches = 0;
+bool g_prof = false;
+struct ProfRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+std::vector<ProfRec> g_prof_recs;
+std::vector<cudaEvent_t> g_event_pool;
+
+void set_error(const char* what, cudaError_t e) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s", what, cudaGetErrorString(e));
+}
+void set_error_text(const char* what) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  snprintf(g_last_error, sizeof(g_last_error), "%s", what);
+}
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Runs `launch` (which enqueues one kernel on `s`), counts it, optionally brackets it
+// with events, and converts a launch error into FCKL_ERR_CUDA.
+template <class F>
+int launch(int kind, cudaStream_t s, const char* what, F&& fn) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  bool prof;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    prof = g_prof;
+    if (prof) {
+      a = take_event();
+      b = take_event();
+    }
+  }
+  if (prof) cudaEventRecord(a, s);
+  fn();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error(what, e);
+    return FCKL_ERR_CUDA;
+  }
+  if (prof) cudaEventRecord(b, s);
+  std::lock_guard<std::mutex> lk(g_mu);
+  ++g_launches;
+  if (prof) g_prof_recs.push_back({kind, a, b});
+  return FCKL_OK;
+}
+
+// ------------------------------------------------------------------ device info
+struct DevInfo {
+  bool init = false;
+  int id = 0, sms = 0, major = 0, minor = 0;
+  bool pre_attr_done = false;
+};
+DevInfo g_dev[64];
+
+int device_info(DevInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_error("cudaGetDevice", e);
+    return FCKL_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= 64) return FCKL_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.init) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      snprintf(g_last_error, sizeof(g_last_error), "cudaDeviceGetAttribute failed");
+      return FCKL_ERR_CUDA;
+    }
+    d.id = dev;
+    d.init = true;
+  }
+  *out = &d;
+  if (d.major != 10 || d.minor != 3) return FCKL_ERR_UNSUPPORTED;
+  return FCKL_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D map over a row-major [dim1][dim0] array with row pitch `pitch_bytes`, 128-byte
+// swizzle, zero fill outside the array.
+int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t dim0, uint64_t dim1,
+             uint64_t pitch_bytes, uint32_t box0, uint32_t box1) {
+  auto enc = encode_fn();
+  if (!enc) {
+    set_error_text("cuTensorMapEncodeTiled entry point not found");
+    return FCKL_ERR_CUDA;
+  }
+  cuuint64_t gdim[2] = {dim0, dim1};
+  cuuint64_t gstride[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box0, box1};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), gdim, gstride, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    snprintf(g_last_error, sizeof(g_last_error),
+             "cuTensorMapEncodeTiled failed (%d): dims %llu x %llu pitch %llu box %u x %u", static_cast<int>(r),
+             static_cast<unsigned long long>(dim0), static_cast<unsigned long long>(dim1),
+             static_cast<unsigned long long>(pitch_bytes), box0, box1);
+    return FCKL_ERR_CUDA;
+  }
+  return FCKL_OK;
+}
+
+// ------------------------------------------------------------------ plan / workspace
+constexpr int VOCAB_TILE = 256;  // BN of the two logits kernels
+constexpr int MAX_SPLITS = 4;    // K-splits of the dH product
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t rup(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+
+struct Plan {
+  int64_t N;
+  int d, V, K, chunk, dt;
+  int rows_alloc;  // chunk rounded up to the 128-row tile
+  int tiles_v;     // vocabulary tiles of 256
+  int ldG;         // row pitch (elements) of the bf16 gradient slab
+  int bn_d;        // N-tile of the dH / dW products
+  size_t off_status, off_sidx, off_sp, off_S, off_T, off_pm, off_pl, off_pc, off_rowloss, off_G, off_dhp,
+      off_Hb, off_Wb, total;
+};
+
+int choose_bn(int d) {
+  if (d % 256 == 0) return 256;
+  if (d % 192 == 0) return 192;
+  if (d % 128 == 0) return 128;
+  return 256;
+}
+
+int check_shape(int64_t N, int d, int V, int K, int chunk, int dt) {
+  if (N < 1 || d < 1 || V < 1 || K < 1 || chunk < 1) return FCKL_ERR_ARG;
+  if (dt != FCKL_BF16 && dt != FCKL_F32) return FCKL_ERR_ARG;
+  if (K > V || K > K_LIMIT) return FCKL_ERR_UNSUPPORTED;
+  if (d % 8 != 0) return FCKL_ERR_UNSUPPORTED;
+  if (N > (int64_t(1) << 40) || V > (1 << 30) || d > (1 << 20)) return FCKL_ERR_UNSUPPORTED;
+  return FCKL_OK;
+}
+
+Plan make_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
+  Plan p{};
+  p.N = N;
+  p.d = d;
+  p.V = V;
+  p.K = K;
+  p.chunk = static_cast<int>(std::min<int64_t>(chunk, N));
+  p.dt = dt;
+  p.rows_alloc = static_cast<int>(rup(p.chunk, BM));
+  p.tiles_v = static_cast<int>(cdiv(V, VOCAB_TILE));
+  p.ldG = static_cast<int>(rup(V, 8));
+  p.bn_d = choose_bn(d);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t r = o;
+    o = static_cast<size_t>(rup(static_cast<int64_t>(o + bytes), 1024));
+    return r;
+  };
+  const size_t R = p.rows_alloc;
+  p.off_status = take(256);
+  p.off_sidx = take(R * K * 4);
+  p.off_sp = take(R * K * 4);
+  p.off_S = take(R * 4);
+  p.off_T = take(R * 4);
+  p.off_pm = take(static_cast<size_t>(p.tiles_v) * R * 4);
+  p.off_pl = take(static_cast<size_t>(p.tiles_v) * R * 4);
+  p.off_pc = take(static_cast<size_t>(p.tiles_v) * R * 4);
+  p.off_rowloss = take(static_cast<size_t>(N) * 4);
+  p.off_G = take(R * p.ldG * 2);
+  p.off_dhp = take(static_cast<size_t>(MAX_SPLITS) * R * d * 4);
+  p.off_Hb = dt == FCKL_F32 ? take(R * d * 2) : o;
+  p.off_Wb = dt == FCKL_F32 ? take(static_cast<size_t>(V) * d * 2) : o;
+  p.total = o;
+  return p;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ------------------------------------------------------------------ kernel launchers
+template <int BN, bool AMN, bool BMN, int EPI>
+int launch_tc(int kind, DevInfo* di, const TcParams& p, cudaStream_t s, const char* what) {
+  auto k = tc_gemm_kernel<BN, AMN, BMN, EPI>;
+  constexpr uint32_t smem = TcSmem<BN>::DYN_BYTES;
+  static_assert(smem <= 232448, "shared memory budget");
+  static bool attr_done[64] = {};  // one flag per device for this instantiation
+  const int dev = di->id;
+  if (!attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) {
+      set_error("cudaFuncSetAttribute", e);
+      return FCKL_ERR_CUDA;
+    }
+    attr_done[dev] = true;
+  }
+  const int grid = static_cast<int>(std::min<int64_t>(p.num_units, di->sms));
+  return launch(kind, s, what, [&] { k<<<grid, NUM_THREADS, smem, s>>>(p); });
+}
+
+template <bool AMN, bool BMN, int EPI>
+int launch_tc_bn(int bn, int kind, DevInfo* di, const TcParams& p, cudaStream_t s, const char* what) {
+  switch (bn) {
+    case 256: return launch_tc<256, AMN, BMN, EPI>(kind, di, p, s, what);
+    case 192: return launch_tc<192, AMN, BMN, EPI>(kind, di, p, s, what);
+    default: return launch_tc<128, AMN, BMN, EPI>(kind, di, p, s, what);
+  }
+}
+
+int launch_cvt(const float* src, void* dst, int64_t n, DevInfo* di, cudaStream_t s) {
+  const int grid = static_cast<int>(std::min<int64_t>(cdiv(n / 4, 256), int64_t(di->sms) * 8));
+  return launch(KIND_CVT, s, "cvt_bf16", [&] {
+    cvt_bf16_kernel<<<std::max(grid, 1), 256, 0, s>>>(src, static_cast<__nv_bfloat16*>(dst), n);
+  });
+}
+
+int launch_preprocess(const Plan& pl, const int32_t* idx, const float* logp, int rows, uint8_t* w, unsigned* status,
+                      DevInfo* di, cudaStream_t s) {
+  const int blocks = static_cast<int>(cdiv(rows, PRE_WARPS));
+  const size_t smem = static_cast<size_t>(PRE_WARPS) * pl.K * 8;
+  if (smem > 48 * 1024) {
+    if (!di->pre_attr_done) {
+      cudaError_t e = cudaFuncSetAttribute(preprocess_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(PRE_WARPS * K_LIMIT * 8));
+      if (e != cudaSuccess) {
+        set_error("cudaFuncSetAttribute(preprocess)", e);
+        return FCKL_ERR_CUDA;
+      }
+      di->pre_attr_done = true;
+    }
+  }
+  return launch(KIND_PREPROCESS, s, "preprocess", [&] {
+    preprocess_kernel<<<blocks, 32 * PRE_WARPS, smem, s>>>(
+        idx, logp, rows, pl.K, pl.V, reinterpret_cast<int*>(w + pl.off_sidx), reinterpret_cast<float*>(w + pl.off_sp),
+        reinterpret_cast<float*>(w + pl.off_S), reinterpret_cast<float*>(w + pl.off_T), status);
+  });
+}
+
+int common_checks(const void* H, const void* W, int dt, const int32_t* idx, const float* logp, int64_t N, int d,
+                  int V, int K, int chunk, void* ws, size_t ws_bytes, Plan* pl, DevInfo** di) {
+  int st = check_shape(N, d, V, K, chunk, dt);
+  if (st) return st;
+  if (!H || !W || !idx || !logp || !ws) return FCKL_ERR_ARG;
+  if (!aligned(H, 16) || !aligned(W, 16) || !aligned(ws, 256) || !aligned(idx, 4) || !aligned(logp, 4))
+    return FCKL_ERR_ARG;
+  *pl = make_plan(N, d, V, K, chunk, dt);
+  if (ws_bytes < pl->total) return FCKL_ERR_WORKSPACE;
+  return device_info(di);
+}
+
+}  // namespace
+}  // namespace fckl
+
+using namespace fckl;
+
+extern "C" {
+
+size_t fckl_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype) {
+  if (check_shape(N, d, V, K, chunk, dtype) != FCKL_OK) return 0;
+  return make_plan(N, d, V, K, chunk, dtype).total;
+}
+
+int fckl_forward(const void* H, const void* W, int dtype, const int32_t* idx, const float* logp, int64_t N, int d,
+                 int V, int K, int chunk, float* loss, float* lse, float* row_loss, void* ws, size_t ws_bytes,
+                 void* stream) {
+  Plan pl;
+  DevInfo* di = nullptr;
+  int st = common_checks(H, W, dtype, idx, logp, N, d, V, K, chunk, ws, ws_bytes, &pl, &di);
+  if (st) return st;
+  if (!loss || !lse || !aligned(loss, 4) || !aligned(lse, 4) || !aligned(row_loss, 4)) return FCKL_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  float* rl = row_loss ? row_loss : reinterpret_cast<float*>(w + pl.off_rowloss);
+  unsigned* status = reinterpret_cast<unsigned*>(w + pl.off_status);
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) {
+    set_error("cudaMemsetAsync", e);
+    return FCKL_ERR_CUDA;
+  }
+  const void* Wb = W;
+  if (dtype == FCKL_F32) {
+    if ((st = launch_cvt(static_cast<const float*>(W), w + pl.off_Wb, int64_t(V) * d, di, s))) return st;
+    Wb = w + pl.off_Wb;
+  }
+  CUtensorMap tmW;
+  if ((st = make_map(&tmW, Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK, VOCAB_TILE))) return st;
+  const size_t esz = dtype == FCKL_F32 ? 4 : 2;
+  for (int64_t r0 = 0; r0 < N; r0 += pl.chunk) {
+    const int rows = static_cast<int>(std::min<int64_t>(pl.chunk, N - r0));
+    if ((st = launch_preprocess(pl, idx + r0 * K, logp + r0 * K, rows, w, status, di, s))) return st;
+    const void* Hc = static_cast<const uint8_t*>(H) + static_cast<size_t>(r0) * d * esz;
+    if (dtype == FCKL_F32) {
+      if ((st = launch_cvt(static_cast<const float*>(Hc), w + pl.off_Hb, int64_t(rows) * d, di, s))) return st;
+      Hc = w + pl.off_Hb;
+    }
+    TcParams p;
+    memset(&p, 0, sizeof(p));
+    if ((st = make_map(&p.tmA, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM))) return st;
+    p.tmB = tmW;
+    p.sch = {static_cast<int>(cdiv(rows, BM)), pl.tiles_v, static_cast<int>(cdiv(d, BK)), 1,
+             static_cast<int>(cdiv(d, BK)), 1};
+    p.num_units = p.sch.m_blocks * p.sch.n_blocks;
+    p.status = status;
+    p.rows_valid = rows;
+    p.V = V;
+    p.K = K;
+    p.sidx = reinterpret_cast<const int*>(w + pl.off_sidx);
+    p.sp = reinterpret_cast<const float*>(w + pl.off_sp);
+    p.S = reinterpret_cast<const float*>(w + pl.off_S);
+    p.pm = reinterpret_cast<float*>(w + pl.off_pm);
+    p.pl = reinterpret_cast<float*>(w + pl.off_pl);
+    p.pc = reinterpret_cast<float*>(w + pl.off_pc);
+    p.ld_part = pl.rows_alloc;
+    if ((st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_STATS>(KIND_FWD_LOGITS, di, p, s, "fwd_logits_lse")))
+      return st;
+    const int cblocks = static_cast<int>(cdiv(rows, 32));
+    if ((st = launch(KIND_FWD_COMBINE, s, "fwd_combine", [&] {
+           combine_kernel<<<cblocks, 256, 0, s>>>(p.pm, p.pl, p.pc, pl.rows_alloc, pl.tiles_v, rows, p.S,
+                                                  reinterpret_cast<const float*>(w + pl.off_T), lse + r0, rl + r0);
+         })))
+      return st;
+  }
+  return launch(KIND_LOSS_REDUCE, s, "loss_reduce", [&] {
+    loss_reduce_kernel<<<1, 1024, 0, s>>>(rl, N, loss);
+  });
+}
+
+int fckl_backward(const void* H, const void* W, int dtype, const int32_t* idx, const float* logp, const float* lse,
+                  int64_t N, int d, int V, int K, int chunk, float grad_scale, void* dH, float* dW, void* ws,
+                  size_t ws_bytes, void* stream) {
+  Plan pl;
+  DevInfo* di = nullptr;
+  int st = common_checks(H, W, dtype, idx, logp, N, d, V, K, chunk, ws, ws_bytes, &pl, &di);
+  if (st) return st;
+  if (!lse || !dH || !dW || !aligned(lse, 4) || !aligned(dH, 16) || !aligned(dW, 16)) return FCKL_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  unsigned* status = reinterpret_cast<unsigned*>(w + pl.off_status);
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) {
+    set_error("cudaMemsetAsync", e);
+    return FCKL_ERR_CUDA;
+  }
+  const void* Wb = W;
+  if (dtype == FCKL_F32) {
+    if ((st = launch_cvt(static_cast<const float*>(W), w + pl.off_Wb, int64_t(V) * d, di, s))) return st;
+    Wb = w + pl.off_Wb;
+  }
+  const int bn = pl.bn_d;
+  CUtensorMap tmW_k, tmW_mn, tmDW;
+  if ((st = make_map(&tmW_k, Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK, VOCAB_TILE))) return st;
+  if ((st = make_map(&tmW_mn, Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, 64, BK))) return st;
+  if ((st = make_map(&tmDW, dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, V, uint64_t(d) * 4, 32, 32))) return st;
+  void* G = w + pl.off_G;
+  float* dhp = reinterpret_cast<float*>(w + pl.off_dhp);
+  const size_t esz = dtype == FCKL_F32 ? 4 : 2;
+  const int kb_v = static_cast<int>(cdiv(V, BK));
+
+  for (int64_t r0 = 0; r0 < N; r0 += pl.chunk) {
+    const int rows = static_cast<int>(std::min<int64_t>(pl.chunk, N - r0));
+    const int mbr = static_cast<int>(cdiv(rows, BM));
+    if ((st = launch_preprocess(pl, idx + r0 * K, logp + r0 * K, rows, w, status, di, s))) return st;
+    const void* Hc = static_cast<const uint8_t*>(H) + static_cast<size_t>(r0) * d * esz;
+    if (dtype == FCKL_F32) {
+      if ((st = launch_cvt(static_cast<const float*>(Hc), w + pl.off_Hb, int64_t(rows) * d, di, s))) return st;
+      Hc = w + pl.off_Hb;
+    }
+    // --- G = scale * (S softmax(z) - p_sparse) for the chunk, z recomputed
+    TcParams pg;
+    memset(&pg, 0, sizeof(pg));
+    if ((st = make_map(&pg.tmA, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM))) return st;
+    pg.tmB = tmW_k;
+    if ((st = make_map(&pg.tmC, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, uint64_t(pl.ldG) * 2, 64, 32)))
+      return st;
+    pg.sch = {mbr, pl.tiles_v, static_cast<int>(cdiv(d, BK)), 1, static_cast<int>(cdiv(d, BK)), 1};
+    pg.num_units = mbr * pl.tiles_v;
+    pg.status = status;
+    pg.rows_valid = rows;
+    pg.V = V;
+    pg.K = K;
+    pg.sidx = reinterpret_cast<const int*>(w + pl.off_sidx);
+    pg.sp = reinterpret_cast<const float*>(w + pl.off_sp);
+    pg.S = reinterpret_cast<const float*>(w + pl.off_S);
+    pg.lse = lse + r0;
+    pg.gscale = grad_scale;
+    pg.c_xlim = V;
+    pg.c_ylim = rows;
+    if ((st = launch_tc<VOCAB_TILE, false, false, EPI_LOGIT_GRAD>(KIND_BWD_GRAD, di, pg, s, "bwd_logit_grad")))
+      return st;
+
+    // --- dH_chunk = G W, split over the vocabulary into fp32 partials
+    const int nbd = static_cast<int>(cdiv(d, bn));
+    const int tiles = mbr * nbd;
+    int splits = 1;
+    {
+      double best = -1.0;
+      for (int sp = 1; sp <= MAX_SPLITS && sp <= kb_v; ++sp) {
+        const int kbps = static_cast<int>(cdiv(kb_v, sp));
+        if (cdiv(kb_v, kbps) != sp) continue;
+        const int64_t units = int64_t(tiles) * sp;
+        const double eff = double(units) / double(cdiv(units, di->sms) * di->sms);
+        if (eff > best + 0.02) {
+          best = eff;
+          splits = sp;
+        }
+      }
+    }
+    TcParams ph;
+    memset(&ph, 0, sizeof(ph));
+    if ((st = make_map(&ph.tmA, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, uint64_t(pl.ldG) * 2, BK, BM)))
+      return st;
+    ph.tmB = tmW_mn;
+    if ((st = make_map(&ph.tmC, dhp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, uint64_t(splits) * pl.rows_alloc,
+                       uint64_t(d) * 4, 32, 32)))
+      return st;
+    const int kbps = static_cast<int>(cdiv(kb_v, splits));
+    ph.sch = {mbr, nbd, kb_v, splits, kbps, 0};
+    ph.num_units = tiles * splits;
+    ph.status = status;
+    ph.c_split_rows = pl.rows_alloc;
+    ph.c_reduce = 0;
+    ph.c_xlim = d;
+    ph.c_ylim = splits * pl.rows_alloc;
+    if ((st = launch_tc_bn<false, true, EPI_STORE_F32>(bn, KIND_BWD_DH, di, ph, s, "bwd_dH_gemm"))) return st;
+    {
+      const int64_t n4 = int64_t(rows) * d / 4;
+      const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(n4, 256), int64_t(di->sms) * 8)));
+      const int64_t stride = int64_t(pl.rows_alloc) * d;
+      if (dtype == FCKL_F32) {
+        float* out = static_cast<float*>(dH) + static_cast<size_t>(r0) * d;
+        st = launch(KIND_BWD_DH_REDUCE, s, "bwd_dH_reduce",
+                    [&] { dh_reduce_kernel<float><<<grid, 256, 0, s>>>(dhp, splits, stride, rows, d, out); });
+      } else {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(dH) + static_cast<size_t>(r0) * d;
+        st = launch(KIND_BWD_DH_REDUCE, s, "bwd_dH_reduce", [&] {
+          dh_reduce_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(dhp, splits, stride, rows, d, out);
+        });
+      }
+      if (st) return st;
+    }
+
+    // --- dW (+)= G^T H_chunk
+    TcParams pw;
+    memset(&pw, 0, sizeof(pw));
+    if ((st = make_map(&pw.tmA, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, uint64_t(pl.ldG) * 2, 64, BK)))
+      return st;
+    if ((st = make_map(&pw.tmB, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, 64, BK))) return st;
+    pw.tmC = tmDW;
+    const int kb_r = static_cast<int>(cdiv(rows, BK));
+    pw.sch = {static_cast<int>(cdiv(V, BM)), nbd, kb_r, 1, kb_r, 0};
+    pw.num_units = pw.sch.m_blocks * nbd;
+    pw.status = status;
+    pw.c_split_rows = 0;
+    pw.c_reduce = r0 > 0 ? 1 : 0;
+    pw.c_xlim = d;
+    pw.c_ylim = V;
+    if ((st = launch_tc_bn<true, true, EPI_STORE_F32>(bn, KIND_BWD_DW, di, pw, s, "bwd_dW_gemm"))) return st;
+  }
+  return FCKL_OK;
+}
+
+int fckl_check(void* ws, void* stream) {
+  if (!ws) return FCKL_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned word = 0;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(unsigned), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    set_error("fckl_check", e);
+    return FCKL_ERR_CUDA;
+  }
+  if (word & ST_TIMEOUT) return FCKL_ERR_TIMEOUT;
+  if (word & ST_BAD_INDEX) return FCKL_ERR_INDEX;
+  return FCKL_OK;
+}
+
+const char* fckl_status_string(int status) {
+  switch (status) {
+    case FCKL_OK: return "ok";
+    case FCKL_ERR_ARG: return "invalid argument (size, null or misaligned pointer)";
+    case FCKL_ERR_INDEX: return "teacher id outside [0, V)";
+    case FCKL_ERR_CUDA: return "CUDA error (see fckl_last_error)";
+    case FCKL_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case FCKL_ERR_WORKSPACE: return "workspace smaller than fckl_workspace_bytes()";
+    case FCKL_ERR_UNSUPPORTED: return "unsupported shape or device (needs sm_103, d % 8 == 0, K <= min(V, 1024))";
+    default: return "unknown status";
+  }
+}
+
+const char* fckl_last_error(void) { return g_last_error; }
+
+int64_t fckl_launch_count(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_launches;
+}
+
+int fckl_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_prof = on != 0;
+  return FCKL_OK;
+}
+
+int fckl_profile_read(double* ms, int64_t* launches, int n_kinds) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    set_error("cudaDeviceSynchronize", e);
+    return FCKL_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (const ProfRec& r : g_prof_recs) {
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess && r.kind < n_kinds) {
+      if (ms) ms[r.kind] += t;
+      if (launches) launches[r.kind] += 1;
+    }
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  g_prof_recs.clear();
+  return FCKL_OK;
+}
+
+const char* fckl_kernel_name(int kind) {
+  if (kind < 0 || kind >= KIND_COUNT) return nullptr;
+  return kKindNames[kind];
+}
+
+}  // extern "C"

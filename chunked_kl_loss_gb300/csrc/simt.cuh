@@ -1,0 +1,164 @@
+// SIMT kernels around the tensor-core steps: teacher-cache preparation, the merge of the
+// per-vocabulary-tile statistics into lse and the per-position loss, the fixed-order loss
+// sum, the split-K sum of dH, and fp32 -> bf16 rounding of fp32 inputs.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "tc_gemm.cuh"
+
+namespace fckl {
+
+constexpr int PRE_WARPS = 4;
+constexpr int K_LIMIT = 1024;
+
+// One warp per position of the chunk. Validates the teacher ids, orders the K slots by
+// (id, slot) so the epilogues can walk them with a cursor, and forms p = exp(logp),
+// S_n = sum_k p_nk and T_n = sum_k p_nk logp_nk (0 log 0 = 0). The cache holds the
+// teacher's top-K log-probabilities without renormalisation, so S_n < 1.
+__global__ void __launch_bounds__(32 * PRE_WARPS) preprocess_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ logp, int rows, int K, int V,
+    int* __restrict__ sidx, float* __restrict__ sp, float* __restrict__ S, float* __restrict__ T,
+    unsigned* __restrict__ status) {
+  extern __shared__ int pre_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * PRE_WARPS + warp;
+  if (row >= rows) return;  // warp-uniform; no block barrier below
+  int* ids = pre_smem + warp * K;
+  float* lps = reinterpret_cast<float*>(pre_smem + PRE_WARPS * K) + warp * K;
+  const int32_t* ri = idx + static_cast<size_t>(row) * K;
+  const float* rl = logp + static_cast<size_t>(row) * K;
+  int bad = 0;
+  for (int k = lane; k < K; k += 32) {
+    const int i = ri[k];
+    ids[k] = i;
+    lps[k] = rl[k];
+    bad |= (i < 0) | (i >= V);
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(status, ST_BAD_INDEX);
+  __syncwarp();
+  float s = 0.f, t = 0.f;
+  for (int k = lane; k < K; k += 32) {
+    const float lp = lps[k];
+    const float pk = expf(lp);
+    const int key = ids[k];
+    int r = 0;
+    for (int j = 0; j < K; ++j) {
+      const int o = ids[j];
+      r += (o < key) | ((o == key) & (j < k));
+    }
+    sidx[static_cast<size_t>(row) * K + r] = key;
+    sp[static_cast<size_t>(row) * K + r] = pk;
+    s += pk;
+    t += (pk > 0.f) ? pk * lp : 0.f;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    t += __shfl_xor_sync(0xffffffffu, t, o);
+  }
+  if (lane == 0) {
+    S[row] = s;
+    T[row] = t;
+  }
+}
+
+// Merge the (m, l, c) statistics of every vocabulary tile of a position:
+//   lse_n  = M + log sum_t l_t exp(m_t - M),   c_n = sum_t c_t
+//   loss_n = T_n - c_n + S_n lse_n             (= sum_k p_nk (logp_nk - z_{n,idx_nk} + lse_n))
+// 32 positions per block; 8 warps split the tiles and are merged in a fixed order.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
+                                                      const float* __restrict__ pc, int ld, int tiles, int rows,
+                                                      const float* __restrict__ S, const float* __restrict__ T,
+                                                      float* __restrict__ lse_out, float* __restrict__ loss_out) {
+  __shared__ float sm[8][32], sl[8][32], sc[8][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int row = blockIdx.x * 32 + lane;
+  const bool valid = row < rows;
+  float M = -INFINITY, Lr = 0.f, C = 0.f;
+  if (valid) {
+    for (int t = w; t < tiles; t += 8) {
+      const size_t o = static_cast<size_t>(t) * ld + row;
+      const float m = pm[o], l = pl[o];
+      const float nm = fmaxf(M, m);
+      Lr = Lr * expf(M - nm) + l * expf(m - nm);
+      M = nm;
+      C += pc[o];
+    }
+  }
+  sm[w][lane] = M;
+  sl[w][lane] = Lr;
+  sc[w][lane] = C;
+  __syncthreads();
+  if (w == 0 && valid) {
+    for (int j = 1; j < 8; ++j) {
+      const float m = sm[j][lane];
+      if (m == -INFINITY) continue;
+      const float nm = fmaxf(M, m);
+      Lr = Lr * expf(M - nm) + sl[j][lane] * expf(m - nm);
+      M = nm;
+      C += sc[j][lane];
+    }
+    const float lse = M + logf(Lr);
+    lse_out[row] = lse;
+    loss_out[row] = T[row] - C + S[row] * lse;
+  }
+}
+
+// Sum of the per-position losses in a fixed order, in fp64.
+__global__ void __launch_bounds__(1024) loss_reduce_kernel(const float* __restrict__ row_loss, int64_t n,
+                                                           float* __restrict__ loss) {
+  __shared__ double sh[1024];
+  double s = 0.0;
+  for (int64_t i = threadIdx.x; i < n; i += 1024) s += static_cast<double>(row_loss[i]);
+  sh[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = 512; o > 0; o >>= 1) {
+    if (threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *loss = static_cast<float>(sh[0]);
+}
+
+__device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
+  uint2 u;
+  u.x = pack_bf16x2(v.x, v.y);
+  u.y = pack_bf16x2(v.z, v.w);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+// dH[row] = sum over K-splits of the fp32 partial products, in split order, stored in
+// the type of H. part is [splits][split_rows][d]; d % 4 == 0.
+template <typename OutT>
+__global__ void __launch_bounds__(256) dh_reduce_kernel(const float* __restrict__ part, int splits,
+                                                        int64_t split_stride, int rows, int d,
+                                                        OutT* __restrict__ out) {
+  const int64_t n4 = static_cast<int64_t>(rows) * d / 4;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = i * 4;
+    float4 a = *reinterpret_cast<const float4*>(part + e);
+    for (int s = 1; s < splits; ++s) {
+      const float4 b = *reinterpret_cast<const float4*>(part + s * split_stride + e);
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    store4(out + e, a);
+  }
+}
+
+// fp32 -> bf16, round to nearest even; n % 4 == 0.
+__global__ void __launch_bounds__(256) cvt_bf16_kernel(const float* __restrict__ src,
+                                                       __nv_bfloat16* __restrict__ dst, int64_t n) {
+  const int64_t n4 = n / 4;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    store4(dst + 4 * i, *reinterpret_cast<const float4*>(src + 4 * i));
+  }
+}
+
+}  // namespace fckl

@@ -1,0 +1,454 @@
+// Persistent, warp-specialised tcgen05 GEMM engine for the fused chunked KL loss.
+//
+// One CTA per SM (1-CTA MMA, 128 x BN tiles, K-blocks of 64 bf16), 192 threads:
+//   warp 0     : TMA producer (one lane) filling a STAGES-deep shared-memory ring
+//   warp 1     : TMEM owner and MMA issuer (one lane); two TMEM accumulators of 128 x 256
+//                fp32 so the epilogue of one tile overlaps the main loop of the next
+//   warps 2..5 : epilogue, one TMEM lane quarter (32 rows) each
+// Work units (tile, K-split) are dealt round-robin over the persistent CTAs in an order
+// chosen by the host so that concurrently running CTAs share operand tiles in L2.
+//
+// Epilogues (the steps of the method that follow each projection):
+//   EPI_FWD_STATS : per-row online max / sum-exp over the tile's vocabulary columns and
+//                   the gather of the logits at the teacher's cached ids; writes one
+//                   (m, l, c) triple per row and vocabulary tile ("Fused, chunked KL loss":
+//                   fold the chunk's logits into the running loss, then drop them)
+//   EPI_LOGIT_GRAD: G = scale * (S_n exp(z - lse_n) - p at the cached ids), rounded to
+//                   bf16 and stored with TMA (the backward pass recomputes the chunk)
+//   EPI_STORE_F32 : fp32 tile stored, or reduce-added, with TMA (dH partials, dW)
+// Every wait is bounded by WAIT_TIMEOUT_NS; on expiry the CTA records FCKL status bit
+// ST_TIMEOUT, lets its copies and MMAs in flight drain, frees TMEM and returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <climits>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace fckl {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int EPI_WARPS = 4;
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_STRIDE = 256;  // TMEM column offset of the second accumulator
+constexpr uint32_t EPI_BUF_BYTES = 4096;  // 32 rows x 128 B staging box per epilogue warp
+constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;
+constexpr float LOG2E = 1.4426950408889634f;
+
+enum : unsigned { ST_BAD_INDEX = 1u, ST_TIMEOUT = 2u };
+enum { EPI_FWD_STATS = 0, EPI_LOGIT_GRAD = 1, EPI_STORE_F32 = 2 };
+
+struct Sched {
+  int m_blocks, n_blocks, k_blocks;
+  int splits, kb_per_split;
+  int n_outer;  // 1: unit order is (split, n, m) with m fastest; 0: (split, m, n) with n fastest
+};
+
+struct TcParams {
+  CUtensorMap tmA;  // operand A (M x K)
+  CUtensorMap tmB;  // operand B (N x K)
+  CUtensorMap tmC;  // epilogue output
+  Sched sch;
+  int num_units;
+  unsigned* status;
+  // logits epilogues
+  int rows_valid, V, K;
+  const int* sidx;   // [rows][K] teacher ids of the chunk, ascending per row
+  const float* sp;   // [rows][K] matching teacher probabilities
+  const float* S;    // [rows] kept teacher mass
+  const float* lse;  // [rows] log-partition (backward)
+  float gscale;
+  float* pm;
+  float* pl;
+  float* pc;
+  int ld_part;
+  // fp32 store epilogue
+  int c_split_rows;  // rows between the slabs of successive K-splits in tmC
+  int c_reduce;      // 1: reduce-add into tmC, 0: plain store
+  int c_xlim, c_ylim;  // extent of tmC: boxes starting at or past it are not issued
+};
+
+template <int BN>
+struct TcSmem {
+  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t EPI_OFF = STAGES * STAGE_BYTES;
+  static constexpr uint32_t BAR_OFF = EPI_OFF + EPI_WARPS * 2 * EPI_BUF_BYTES;
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 + 2 + 1;
+  static constexpr uint32_t END = BAR_OFF + NUM_BARS * 8 + 16;
+  static constexpr uint32_t DYN_BYTES = END + 1024;  // slack for 1024-byte alignment
+};
+
+__device__ __forceinline__ void decode_unit(const Sched& s, int u, int& mb, int& nb, int& sp, int& kb0,
+                                            int& kb1) {
+  const int tiles = s.m_blocks * s.n_blocks;
+  sp = u / tiles;
+  const int r = u - sp * tiles;
+  if (s.n_outer) {
+    nb = r / s.m_blocks;
+    mb = r - nb * s.m_blocks;
+  } else {
+    mb = r / s.n_blocks;
+    nb = r - mb * s.n_blocks;
+  }
+  kb0 = sp * s.kb_per_split;
+  kb1 = min(s.k_blocks, kb0 + s.kb_per_split);
+}
+
+// Bounded wait on one mbarrier phase, polled by the calling thread. Returns false when the
+// CTA is aborting (another role gave up) or when the deadline passed (then it also raises
+// the abort flag and the status bit).
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                           unsigned* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > WAIT_TIMEOUT_NS) {
+        *abort_flag = 1;
+        atomicOr(status, ST_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Same, for teardown: ignores the abort flag, still bounded.
+__device__ __forceinline__ bool drain_phase(uint64_t* bar, uint32_t parity, unsigned* status) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 31u && globaltimer_ns() - t0 > WAIT_TIMEOUT_NS) {
+      atomicOr(status, ST_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Warp-uniform wait: lane 0 polls, the verdict is broadcast.
+__device__ __forceinline__ bool warp_wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                unsigned* status) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_phase(bar, parity, abort_flag, status) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// First slot k of a row's ascending id list with ids[k] >= key.
+__device__ __forceinline__ int lower_bound_ids(const int* ids, int n, int key) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(ids + mid) < key)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+// x[pos] for a runtime pos in [0, 32) without leaving registers.
+__device__ __forceinline__ float pick32(const float (&x)[32], int pos) {
+  float r = 0.f;
+#pragma unroll
+  for (int t = 0; t < 32; ++t) r = (t == pos) ? x[t] : r;
+  return r;
+}
+__device__ __forceinline__ void sub32(float (&x)[32], int pos, float v) {
+#pragma unroll
+  for (int t = 0; t < 32; ++t) x[t] = (t == pos) ? x[t] - v : x[t];
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int BN, bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  using L = TcSmem<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], EPI_WARPS);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&p.tmA);
+    prefetch_tmap(&p.tmB);
+    if (EPI != EPI_FWD_STATS) prefetch_tmap(&p.tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t cnt = 0;
+      uint32_t armed = 0, armed_par = 0;  // per stage: ever armed, parity of the last arming
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        int mb, nb, sp, kb0, kb1;
+        decode_unit(p.sch, u, mb, nb, sp, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb, ++cnt) {
+          const uint32_t s = cnt % STAGES, ph = (cnt / STAGES) & 1u;
+          if (!wait_phase(&empty[s], ph ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES);
+          armed |= 1u << s;
+          armed_par = (armed_par & ~(1u << s)) | (ph << s);
+          uint8_t* a = smem + s * L::STAGE_BYTES;
+          uint8_t* b = a + L::A_BYTES;
+          if (!A_MN) {
+            tma_load_2d(a, &p.tmA, &full[s], kb * BK, mb * BM);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j) tma_load_2d(a + j * 8192, &p.tmA, &full[s], mb * BM + 64 * j, kb * BK);
+          }
+          if (!B_MN) {
+            tma_load_2d(b, &p.tmB, &full[s], kb * BK, nb * BN);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(b + j * 8192, &p.tmB, &full[s], nb * BN + 64 * j, kb * BK);
+          }
+        }
+      }
+      // Every copy this thread started must land before the CTA may exit.
+      for (int s = 0; s < STAGES; ++s)
+        if (armed & (1u << s)) drain_phase(&full[s], (armed_par >> s) & 1u, p.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, A_MN, B_MN);
+      uint32_t cnt = 0, it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+        int mb, nb, sp, kb0, kb1;
+        decode_unit(p.sch, u, mb, nb, sp, kb0, kb1);
+        const uint32_t acc = it & 1u, use = it >> 1;
+        if (!wait_phase(&tempty[acc], (use & 1u) ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
+        for (int kb = kb0; kb < kb1; ++kb, ++cnt) {
+          const uint32_t s = cnt % STAGES, ph = (cnt / STAGES) & 1u;
+          if (!wait_phase(&full[s], ph, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + s * L::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + L::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? make_sdesc_sw128(a_addr + kk * 2048, 8192, 1024)
+                                     : make_sdesc_sw128(a_addr + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? make_sdesc_sw128(b_addr + kk * 2048, 8192, 1024)
+                                     : make_sdesc_sw128(b_addr + kk * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+      }
+      // All MMAs issued by this thread must finish before TMEM is released.
+      umma_commit(drain);
+      drain_phase(drain, 0, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    uint8_t* ebuf0 = smem + L::EPI_OFF + (warp - 2) * 2 * EPI_BUF_BYTES;
+    uint32_t it = 0, ecnt = 0;
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
+      int mb, nb, sp, kb0, kb1;
+      decode_unit(p.sch, u, mb, nb, sp, kb0, kb1);
+      const uint32_t acc = it & 1u, use = it >> 1;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * ACC_STRIDE;
+      const int row = mb * BM + 32 * q + lane;
+
+      if constexpr (EPI == EPI_FWD_STATS || EPI == EPI_LOGIT_GRAD) {
+        const bool valid = row < p.rows_valid;
+        const int v0 = nb * BN;
+        const int* ids = p.sidx + static_cast<size_t>(valid ? row : 0) * p.K;
+        const float* pr = p.sp + static_cast<size_t>(valid ? row : 0) * p.K;
+        int k = p.K, nxt = INT_MAX;
+        if (valid) {
+          k = lower_bound_ids(ids, p.K, v0);
+          nxt = k < p.K ? __ldg(ids + k) : INT_MAX;
+        }
+        if constexpr (EPI == EPI_FWD_STATS) {
+          if (!warp_wait_phase(&tfull[acc], use & 1u, abort_flag, p.status)) break;
+          tc_fence_after();
+          float m = -INFINITY, l = 0.f, c = 0.f;
+#pragma unroll 1
+          for (int j = 0; j < BN / 32; ++j) {
+            float x[32];
+            __syncwarp();
+            tmem_ld32(taddr + 32 * j, x);
+            if (j == BN / 32 - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty[acc]);
+            }
+            const int cb = v0 + 32 * j;
+            if (cb + 32 > p.V) {
+#pragma unroll
+              for (int t = 0; t < 32; ++t)
+                if (cb + t >= p.V) x[t] = -INFINITY;
+            }
+            while (nxt < cb + 32) {
+              c = fmaf(__ldg(pr + k), pick32(x, nxt - cb), c);
+              ++k;
+              nxt = k < p.K ? __ldg(ids + k) : INT_MAX;
+            }
+            float cm = x[0];
+#pragma unroll
+            for (int t = 1; t < 32; ++t) cm = fmaxf(cm, x[t]);
+            const float nm = fmaxf(m, cm);
+            const float nml = nm * LOG2E;
+            float s = 0.f;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) s += ex2_approx(fmaf(x[t], LOG2E, -nml));
+            l = fmaf(l, ex2_approx((m - nm) * LOG2E), s);
+            m = nm;
+          }
+          if (valid) {
+            const size_t o = static_cast<size_t>(nb) * p.ld_part + row;
+            p.pm[o] = m;
+            p.pl[o] = l;
+            p.pc[o] = c;
+          }
+        } else {
+          const float a = valid ? p.gscale * __ldg(p.S + row) : 0.f;
+          const float nl = valid ? -__ldg(p.lse + row) * LOG2E : 0.f;
+          if (!warp_wait_phase(&tfull[acc], use & 1u, abort_flag, p.status)) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int jj = 0; jj < BN / 64; ++jj, ++ecnt) {
+            uint8_t* buf = ebuf0 + (ecnt & 1u) * EPI_BUF_BYTES;
+            if (ecnt >= 2 && lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int j = 2 * jj + h;
+              float x[32];
+              __syncwarp();
+              tmem_ld32(taddr + 32 * j, x);
+              if (j == BN / 32 - 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc]);
+              }
+              const int cb = v0 + 32 * j;
+#pragma unroll
+              for (int t = 0; t < 32; ++t) x[t] = a * ex2_approx(fmaf(x[t], LOG2E, nl));
+              while (nxt < cb + 32) {
+                sub32(x, nxt - cb, p.gscale * __ldg(pr + k));
+                ++k;
+                nxt = k < p.K ? __ldg(ids + k) : INT_MAX;
+              }
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc) {
+                uint4 w;
+                w.x = pack_bf16x2(x[8 * cc + 0], x[8 * cc + 1]);
+                w.y = pack_bf16x2(x[8 * cc + 2], x[8 * cc + 3]);
+                w.z = pack_bf16x2(x[8 * cc + 4], x[8 * cc + 5]);
+                w.w = pack_bf16x2(x[8 * cc + 6], x[8 * cc + 7]);
+                const int chunk16 = (4 * h + cc) ^ (lane & 7);
+                *reinterpret_cast<uint4*>(buf + lane * 128 + chunk16 * 16) = w;
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int sx = v0 + 64 * jj, sy = mb * BM + 32 * q;
+              if (sx < p.c_xlim && sy < p.c_ylim) tma_store_2d(&p.tmC, buf, sx, sy);
+              bulk_commit();
+            }
+          }
+        }
+      } else {
+        // EPI_STORE_F32
+        if (!warp_wait_phase(&tfull[acc], use & 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const int y = sp * p.c_split_rows + mb * BM + 32 * q;
+#pragma unroll 1
+        for (int j = 0; j < BN / 32; ++j, ++ecnt) {
+          uint8_t* buf = ebuf0 + (ecnt & 1u) * EPI_BUF_BYTES;
+          if (ecnt >= 2 && lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          float x[32];
+          tmem_ld32(taddr + 32 * j, x);
+          if (j == BN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            const int chunk16 = cc ^ (lane & 7);
+            *reinterpret_cast<float4*>(buf + lane * 128 + chunk16 * 16) =
+                make_float4(x[4 * cc + 0], x[4 * cc + 1], x[4 * cc + 2], x[4 * cc + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int sx = nb * BN + 32 * j;
+            if (sx < p.c_xlim && y < p.c_ylim) {
+              if (p.c_reduce)
+                tma_reduce_add_2d(&p.tmC, buf, sx, y);
+              else
+                tma_store_2d(&p.tmC, buf, sx, y);
+            }
+            bulk_commit();
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace fckl

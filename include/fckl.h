@@ -1,0 +1,116 @@
+/*
+ * fckl.h - C ABI of the fused, chunked top-K KL distillation loss on one GB300 (sm_103a).
+ *
+ * The operation ("Hugging Face：让知识蒸馏廉价到可大规模运行", paragraphs "离线蒸馏" and
+ * "Fused, chunked KL loss"; "Chunkovaná KL strata umožnila destilovať LLM s 32-tisícovým
+ * kontextom na jednom H200", sections "Dva odlišné zdroje úspory" and "Čo dopĺňajú
+ * podrobnejšie experimenty"):
+ *
+ *   z_n    = W h_n                     student logits of position n, never stored whole
+ *   lse_n  = log sum_v exp(z_nv)
+ *   p_nk   = exp(logp_nk),  S_n = sum_k p_nk   (teacher top-K cache, not renormalised)
+ *   loss   = sum_n sum_k p_nk (logp_nk - (z_{n,idx_nk} - lse_n))        (0 log 0 = 0)
+ *   G_n    = S_n softmax(z_n) - p_sparse_n,   dH = G W,   dW = G^T H
+ *
+ * The sequence is walked one chunk of positions at a time: the forward pass projects
+ * a chunk, folds it into the running loss and drops it; the backward pass recomputes
+ * the chunk's logits to form G. Only a chunk x V gradient slab is ever held.
+ *
+ * Conventions for every call below
+ *  - All arrays are dense and row-major. "device" pointers are CUDA device memory of the
+ *    current device; the caller owns every buffer, including the workspace. The library
+ *    allocates no device memory and keeps only host-side caches (device properties).
+ *  - H is [N, d] and W is [V, d], both of type `dtype` (FCKL_BF16 or FCKL_F32). FCKL_F32
+ *    inputs are rounded to bf16 on the device and the tensor-core products run in bf16
+ *    with fp32 accumulation, exactly as for FCKL_BF16 inputs.
+ *  - idx is int32 [N, K]: teacher token ids, any order, each in [0, V). logp is fp32 [N, K]:
+ *    the teacher's log-probabilities for those ids; -inf marks an empty slot. A repeated
+ *    id within a row contributes once per slot.
+ *  - `stream` is a cudaStream_t (may be NULL for the legacy default stream). Every call is
+ *    asynchronous on it; inputs must stay alive and unmodified until the work completes.
+ *  - Limits: N >= 1, 1 <= K <= min(V, 1024), d % 8 == 0 (16-byte rows for the tensor
+ *    memory accelerator), chunk >= 1; H, W, dH and dW 16-byte aligned; ws 256-byte aligned.
+ *  - Return value: FCKL_OK, or an fckl_status naming the first problem found. Argument
+ *    errors launch nothing. Errors found on the device (a teacher id outside [0, V), a
+ *    pipeline wait that ran out) cannot be returned by an asynchronous call: they are
+ *    ORed into a status word in the workspace and read back by fckl_check().
+ *    Results of a call whose status word is not clear are unspecified. No device code
+ *    traps; every wait on the device is bounded in time.
+ */
+#ifndef FCKL_H
+#define FCKL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FCKL_OK = 0,
+    FCKL_ERR_ARG = 1,         /* bad size, null or misaligned pointer */
+    FCKL_ERR_INDEX = 2,       /* a teacher id outside [0, V) (device-detected) */
+    FCKL_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed; see fckl_last_error() */
+    FCKL_ERR_TIMEOUT = 4,     /* a bounded device wait ran out (device-detected) */
+    FCKL_ERR_WORKSPACE = 5,   /* ws_bytes below fckl_workspace_bytes() */
+    FCKL_ERR_UNSUPPORTED = 6  /* shape outside the limits above, or not an sm_103 device */
+} fckl_status;
+
+typedef enum { FCKL_BF16 = 0, FCKL_F32 = 1 } fckl_dtype;
+
+/* Bytes of device workspace that fckl_forward and fckl_backward need for this shape.
+ * The size grows with chunk * V (the gradient slab) and with N only through 4 bytes per
+ * position; 0 if the shape is outside the limits. */
+size_t fckl_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
+
+/* Forward pass.
+ *   loss     : device fp32 [1]  <- sum over positions of the per-position KL (a SUM, not a mean)
+ *   lse      : device fp32 [N]  <- log-partition of every position, kept for fckl_backward
+ *   row_loss : device fp32 [N]  <- per-position KL, or NULL when not wanted
+ * Overwrites the workspace and clears its status word first. */
+int fckl_forward(const void* H, const void* W, int dtype,
+                 const int32_t* idx, const float* logp,
+                 int64_t N, int d, int V, int K, int chunk,
+                 float* loss, float* lse, float* row_loss,
+                 void* ws, size_t ws_bytes, void* stream);
+
+/* Backward pass: recomputes every chunk's logits and forms G from `lse` (as written by
+ * fckl_forward for the same H, W).
+ *   grad_scale : upstream derivative d(objective)/d(loss); multiplies dH and dW
+ *   dH         : device [N, d] of type `dtype`, overwritten
+ *   dW         : device fp32 [V, d], overwritten
+ * Overwrites the workspace and clears its status word first. */
+int fckl_backward(const void* H, const void* W, int dtype,
+                  const int32_t* idx, const float* logp, const float* lse,
+                  int64_t N, int d, int V, int K, int chunk,
+                  float grad_scale, void* dH, float* dW,
+                  void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, returns the status found on the device by the last call that
+ * used `ws` (FCKL_OK if none), and clears it. */
+int fckl_check(void* ws, void* stream);
+
+/* Static text for a status code. */
+const char* fckl_status_string(int status);
+
+/* Text of the last CUDA error seen by this library in this process ("" if none). */
+const char* fckl_last_error(void);
+
+/* Number of kernels this library has launched in this process. */
+int64_t fckl_launch_count(void);
+
+/* Per-kernel timing. While enabled, every launch is bracketed by CUDA events recorded on
+ * its own stream. fckl_profile_read synchronises the device, adds the measured time (ms)
+ * and launch count of each kernel kind into ms[kind] and launches[kind] for kind <
+ * n_kinds, and forgets the events. fckl_kernel_name(kind) names a kind (NULL past the
+ * last). */
+int fckl_profile_enable(int on);
+int fckl_profile_read(double* ms, int64_t* launches, int n_kinds);
+const char* fckl_kernel_name(int kind);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FCKL_H */

@@ -1,0 +1,97 @@
+"""The C ABI library: it loads, exports every function include/fckl.h declares, sizes its
+workspace as documented, and rejects bad arguments before touching a device.
+
+CPU only: no call here reaches a kernel launch.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunked_kl_loss_gb300 as fckl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fckl.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fckl_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(fckl):
+    names = declared_functions()
+    assert "fckl_forward" in names and "fckl_backward" in names
+    lib = ctypes.CDLL(fckl.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(fckl):
+    lib = fckl.load()
+    for st in range(7):
+        assert lib.fckl_status_string(st)
+    assert lib.fckl_status_string(99) == b"unknown status"
+
+
+def test_kernel_names(fckl):
+    names = fckl.kernel_names()
+    assert names[:2] == ["preprocess", "fwd_logits_lse"]
+    assert "bwd_dW_gemm" in names
+
+
+def test_workspace_size_rules(fckl):
+    ws = fckl.workspace_bytes
+    a = ws(32768, 3072, 128256, 100, 2048, fckl.BF16)
+    b = ws(65536, 3072, 128256, 100, 2048, fckl.BF16)
+    c = ws(131072, 3072, 128256, 100, 2048, fckl.BF16)
+    assert a > 2048 * 128256 * 2  # holds at least the bf16 gradient slab of one chunk
+    # grows with N only by 4 bytes per position (per-position losses), rounded to 1 KiB
+    assert abs((b - a) - 32768 * 4) <= 1024 and abs((c - b) - 65536 * 4) <= 1024
+    # the chunk bounds the slab
+    assert ws(32768, 3072, 128256, 100, 4096, fckl.BF16) > a
+    assert ws(32768, 3072, 128256, 100, 1024, fckl.BF16) < a
+    # fp32 inputs need room for their bf16 copies
+    assert ws(64, 256, 4096, 16, 16, fckl.F32) > ws(64, 256, 4096, 16, 16, fckl.BF16)
+    # outside the limits: 0
+    assert ws(0, 256, 4096, 16, 16, fckl.BF16) == 0
+    assert ws(64, 250, 4096, 16, 16, fckl.BF16) == 0  # d % 8 != 0
+    assert ws(64, 256, 16, 17, 16, fckl.BF16) == 0    # K > V
+    assert ws(64, 256, 4096, 1025, 16, fckl.BF16) == 0
+    assert ws(64, 256, 4096, 16, 0, fckl.BF16) == 0
+    assert ws(64, 256, 4096, 16, 16, 7) == 0
+
+
+def test_argument_errors_launch_nothing(fckl):
+    lib = fckl.load()
+    before = lib.fckl_launch_count()
+    p = ctypes.c_void_p(256)  # never dereferenced: the checks fail first
+    z = ctypes.c_void_p(0)
+    # bad sizes
+    assert lib.fckl_forward(p, p, 0, p, p, 0, 256, 4096, 16, 16, p, p, z, p, 1 << 30, z) == fckl.ERR_ARG
+    assert lib.fckl_forward(p, p, 0, p, p, 64, 250, 4096, 16, 16, p, p, z, p, 1 << 30, z) == fckl.ERR_UNSUPPORTED
+    # null input
+    assert lib.fckl_forward(z, p, 0, p, p, 64, 256, 4096, 16, 16, p, p, z, p, 1 << 30, z) == fckl.ERR_ARG
+    # misaligned H
+    assert lib.fckl_forward(ctypes.c_void_p(258), p, 0, p, p, 64, 256, 4096, 16, 16, p, p, z, p, 1 << 30,
+                            z) == fckl.ERR_ARG
+    # workspace too small
+    assert lib.fckl_forward(p, p, 0, p, p, 64, 256, 4096, 16, 16, p, p, z, p, 16, z) == fckl.ERR_WORKSPACE
+    assert lib.fckl_backward(p, p, 0, p, p, p, 64, 256, 4096, 16, 16, ctypes.c_float(1.0), p, p, p, 16,
+                             z) == fckl.ERR_WORKSPACE
+    assert lib.fckl_backward(p, p, 1, p, p, z, 64, 256, 4096, 16, 16, ctypes.c_float(1.0), p, p, p,
+                             1 << 30, z) in (fckl.ERR_ARG, fckl.ERR_CUDA, fckl.ERR_UNSUPPORTED)
+    assert lib.fckl_check(z, z) == fckl.ERR_ARG
+    assert lib.fckl_launch_count() == before
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    import importlib
+    import chunked_kl_loss_gb300 as m
+    monkeypatch.setattr(m, "LIB_PATH", "/nonexistent/libfckl.so")
+    monkeypatch.setattr(m, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        m.load()
+    importlib.reload(m)

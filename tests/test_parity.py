@@ -1,0 +1,132 @@
+"""GPU parity: the CUDA path against the fp64 oracle on the same seeded inputs.
+
+Tolerances (the method's stated bar for bf16 inputs): loss relative error <= 1e-3;
+dH and dW max-abs error <= 2e-2 x max|ref|. lse and the per-position losses are also
+compared (max-abs <= 1e-3 x (1 + |ref|)) as diagnostics of the forward statistics.
+
+Shapes are small enough for the oracle to finish in seconds but span several 128-row and
+256-column tiles, ragged tails in N, V, d and the chunk, and the degenerate cases.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+from oracle import fckl_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+LOSS_RTOL = 1e-3
+GRAD_TOL = 2e-2
+
+
+def to_dev(x, dtype):
+    dev = torch.device("cuda")
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    H = torch.from_numpy(x["H"]).to(dev).to(tdt)
+    W = torch.from_numpy(x["W"]).to(dev).to(tdt)
+    idx = torch.from_numpy(np.ascontiguousarray(x["idx"], dtype=np.int32)).to(dev)
+    logp = torch.from_numpy(np.ascontiguousarray(x["logp"], dtype=np.float32)).to(dev)
+    return H, W, idx, logp
+
+
+def run_gpu(fckl, x, chunk, dtype, grad_scale=1.0):
+    H, W, idx, logp = to_dev(x, dtype)
+    N, d = H.shape
+    V, K = W.shape[0], idx.shape[1]
+    ws = fckl.Workspace(N, d, V, K, chunk, fckl.F32 if dtype == "f32" else fckl.BF16)
+    loss, lse, rl = fckl.forward(H, W, idx, logp, chunk, ws=ws, row_loss=True)
+    assert fckl.check(ws) == fckl.OK
+    dH, dW = fckl.backward(H, W, idx, logp, lse, chunk, grad_scale=grad_scale, ws=ws)
+    assert fckl.check(ws) == fckl.OK
+    return (float(loss.item()), lse.cpu().numpy().astype(np.float64), rl.cpu().numpy().astype(np.float64),
+            dH.float().cpu().numpy().astype(np.float64), dW.cpu().numpy().astype(np.float64))
+
+
+def assert_parity(got, ref_x, chunk, grad_scale=1.0):
+    loss, lse, rl, dH, dW = got
+    r_loss, r_lse, r_rl = orc.forward(ref_x["H"], ref_x["W"], ref_x["idx"], ref_x["logp"], chunk)
+    r_dH, r_dW = orc.backward(ref_x["H"], ref_x["W"], ref_x["idx"], ref_x["logp"], grad_scale, chunk)
+    assert abs(loss - r_loss) <= LOSS_RTOL * abs(r_loss), (loss, r_loss)
+    assert np.abs(lse - r_lse).max() <= 1e-3 * (1 + np.abs(r_lse).max())
+    assert np.abs(rl - r_rl).max() <= 1e-3 * (1 + np.abs(r_rl).max())
+    e_dH = np.abs(dH - r_dH).max() / np.abs(r_dH).max()
+    e_dW = np.abs(dW - r_dW).max() / np.abs(r_dW).max()
+    assert e_dH <= GRAD_TOL, e_dH
+    assert e_dW <= GRAD_TOL, e_dW
+    return e_dH, e_dW
+
+
+def test_tiny_workload_fp32(fckl):
+    """The tiny workload exactly: N=64, d=256, V=4096, K=16, chunk=16, fp32 storage."""
+    w = synthetic.WORKLOADS["tiny_n64_d256_v4096"]
+    x = synthetic.make_inputs(w.N, w.d, w.V, w.K, dtype="f32", seed=0)
+    got = run_gpu(fckl, x, w.chunk, "f32")
+    assert_parity(got, x, w.chunk)
+
+
+@pytest.mark.parametrize("N,d,V,K,chunk", [
+    (300, 320, 5000, 40, 128),    # ragged N, chunk tail of 44 rows, V tail, d tail vs a 256 tile
+    (256, 512, 4096, 16, 256),    # exact tiles
+    (130, 384, 2056, 33, 200),    # chunk not a multiple of 128; d on a 128 N-tile; V % 256 = 8
+    (1, 64, 256, 1, 1),           # one position, one slot
+    (70, 128, 1000, 20, 1000),    # chunk larger than N
+])
+def test_ragged_shapes_bf16(fckl, N, d, V, K, chunk):
+    x = synthetic.make_inputs(N, d, V, K, dtype="bf16", seed=N + d)
+    got = run_gpu(fckl, x, chunk, "bf16", grad_scale=0.75)
+    assert_parity(got, x, chunk, grad_scale=0.75)
+
+
+def test_llama_vocab_slab(fckl):
+    """d=3072, V=128256, K=100 (the 8K-32K workloads' per-position shape) on 256 positions."""
+    x = synthetic.make_inputs(256, 3072, 128256, 100, dtype="bf16", seed=5)
+    got = run_gpu(fckl, x, 128, "bf16")
+    assert_parity(got, x, 128)
+
+
+def test_gptoss_vocab_slab(fckl):
+    """d=2880, V=201088 (192-wide N tiles; V not a multiple of 256) on 192 positions."""
+    x = synthetic.make_inputs(192, 2880, 201088, 100, dtype="bf16", seed=6)
+    got = run_gpu(fckl, x, 128, "bf16")
+    assert_parity(got, x, 128)
+
+
+def test_repeated_ids_and_empty_slots(fckl):
+    x = synthetic.make_inputs(100, 128, 1000, 20, dtype="bf16", seed=7)
+    x["idx"][:, 5] = x["idx"][:, 4]          # a repeated id in every row
+    x["logp"][::3, -1] = -np.inf             # empty slots
+    got = run_gpu(fckl, x, 64, "bf16")
+    assert_parity(got, x, 64)
+
+
+def test_bad_teacher_id_reported(fckl):
+    x = synthetic.make_inputs(40, 64, 512, 8, dtype="bf16", seed=8)
+    x["idx"][3, 2] = 512
+    H, W, idx, logp = to_dev(x, "bf16")
+    ws = fckl.Workspace(40, 64, 512, 8, 16, fckl.BF16)
+    fckl.forward(H, W, idx, logp, 16, ws=ws)
+    assert fckl.check(ws, raise_on_error=False) == fckl.ERR_INDEX
+    # the status word is cleared by the read, and a clean call reports OK
+    assert fckl.check(ws, raise_on_error=False) == fckl.OK
+    x["idx"][3, 2] = 0 if 0 not in x["idx"][3] else 511
+    H, W, idx, logp = to_dev(x, "bf16")
+    fckl.forward(H, W, idx, logp, 16, ws=ws)
+    assert fckl.check(ws, raise_on_error=False) == fckl.OK
+
+
+def test_sum_of_dW_over_vocab_is_zero(fckl):
+    """G rows sum to zero, so sum_v dW[v, :] = 0 up to rounding (holds at any size)."""
+    x = synthetic.make_inputs(512, 256, 8192, 50, dtype="bf16", seed=9)
+    _, _, _, dH, dW = run_gpu(fckl, x, 256, "bf16")
+    col = np.abs(dW.sum(0)).max()
+    assert col <= 1e-2 * np.abs(dW).max() * np.sqrt(8192 / 256)
+
+
+def test_repeat_calls_are_deterministic(fckl):
+    x = synthetic.make_inputs(300, 256, 3000, 30, dtype="bf16", seed=10)
+    a = run_gpu(fckl, x, 128, "bf16")
+    b = run_gpu(fckl, x, 128, "bf16")
+    assert a[0] == b[0]
+    for u, v in zip(a[1:], b[1:]):
+        np.testing.assert_array_equal(u, v)
