@@ -601,3 +601,137 @@ const char* fckl_kernel_name(int kind) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ forward with library-owned scratch
+// For callers that cannot allocate device memory themselves (see fckl_forward_static in
+// include/fckl.h). The scratch is one file-scope device array, reserved on every GPU where
+// this library is loaded until the process exits, and shared by every call on that GPU.
+static __device__ __align__(256) uint8_t g_fckl_static_scratch[FCKL_STATIC_SCRATCH_BYTES];
+
+namespace fckl {
+namespace {
+
+void* g_static_scratch_addr[64] = {};
+
+// Device address of g_fckl_static_scratch on the current device. The host-side name of the
+// array is only a stand-in, never a device address, so the address is looked up once per
+// device, with that device current, and cached.
+int static_scratch_address(int dev, void** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_static_scratch_addr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_fckl_static_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      snprintf(g_last_error, sizeof(g_last_error), "cudaGetSymbolAddress(static scratch): %s",
+               cudaGetErrorString(e));
+      return FCKL_ERR_CUDA;
+    }
+    g_static_scratch_addr[dev] = p;
+  }
+  *out = g_static_scratch_addr[dev];
+  return FCKL_OK;
+}
+
+}  // namespace
+}  // namespace fckl
+
+extern "C" int fckl_forward_static(const void* H, const void* W, int dtype, const int32_t* idx, const float* logp,
+                                   int64_t N, int d, int V, int K, int chunk, float* loss, float* lse,
+                                   float* row_loss, uint32_t* status, void* stream) {
+  int st = check_shape(N, d, V, K, chunk, dtype);
+  if (st) return st;
+  if (dtype != FCKL_BF16) {
+    set_error_text("fckl_forward_static takes bf16 H and W only");
+    return FCKL_ERR_UNSUPPORTED;
+  }
+  if (!H || !W || !idx || !logp || !loss || !lse || !row_loss || !status) return FCKL_ERR_ARG;
+  if (!aligned(H, 16) || !aligned(W, 16) || !aligned(idx, 4) || !aligned(logp, 4) || !aligned(loss, 4) ||
+      !aligned(lse, 4) || !aligned(row_loss, 4) || !aligned(status, 4))
+    return FCKL_ERR_ARG;
+
+  // Forward-only layout inside the static array: status word, ordered cache slots, S, T and
+  // the per-vocabulary-tile statistics of one chunk. The per-position losses go straight
+  // to the caller's row_loss, so nothing here grows with N.
+  Plan pl = make_plan(N, d, V, K, chunk, dtype);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t r = o;
+    o = static_cast<size_t>(rup(static_cast<int64_t>(o + bytes), 1024));
+    return r;
+  };
+  const size_t R = pl.rows_alloc;
+  pl.off_status = take(256);
+  pl.off_sidx = take(R * K * 4);
+  pl.off_sp = take(R * K * 4);
+  pl.off_S = take(R * 4);
+  pl.off_T = take(R * 4);
+  pl.off_pm = take(static_cast<size_t>(pl.tiles_v) * R * 4);
+  pl.off_pl = take(static_cast<size_t>(pl.tiles_v) * R * 4);
+  pl.off_pc = take(static_cast<size_t>(pl.tiles_v) * R * 4);
+  if (o > FCKL_STATIC_SCRATCH_BYTES) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    snprintf(g_last_error, sizeof(g_last_error),
+             "fckl_forward_static: this shape needs %zu bytes of scratch, above the %zu-byte maximum; "
+             "use a smaller chunk or fckl_forward with a workspace",
+             o, static_cast<size_t>(FCKL_STATIC_SCRATCH_BYTES));
+    return FCKL_ERR_WORKSPACE;
+  }
+  DevInfo* di = nullptr;
+  if ((st = device_info(&di))) return st;
+  void* base = nullptr;
+  if ((st = static_scratch_address(di->id, &base))) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(base);
+  unsigned* dstatus = reinterpret_cast<unsigned*>(w + pl.off_status);
+  // The array keeps whatever the previous call left; only the status word must start at 0
+  // (every other region is written before it is read).
+  cudaError_t e = cudaMemsetAsync(dstatus, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) {
+    set_error("cudaMemsetAsync", e);
+    return FCKL_ERR_CUDA;
+  }
+  CUtensorMap tmW;
+  if ((st = make_map(&tmW, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK, VOCAB_TILE))) return st;
+  for (int64_t r0 = 0; r0 < N; r0 += pl.chunk) {
+    const int rows = static_cast<int>(std::min<int64_t>(pl.chunk, N - r0));
+    if ((st = launch_preprocess(pl, idx + r0 * K, logp + r0 * K, rows, w, dstatus, di, s))) return st;
+    const void* Hc = static_cast<const uint8_t*>(H) + static_cast<size_t>(r0) * d * 2;
+    TcParams p;
+    memset(&p, 0, sizeof(p));
+    if ((st = make_map(&p.tmA, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM))) return st;
+    p.tmB = tmW;
+    p.sch = {static_cast<int>(cdiv(rows, BM)), pl.tiles_v, static_cast<int>(cdiv(d, BK)), 1,
+             static_cast<int>(cdiv(d, BK)), 1};
+    p.num_units = p.sch.m_blocks * p.sch.n_blocks;
+    p.status = dstatus;
+    p.rows_valid = rows;
+    p.V = V;
+    p.K = K;
+    p.sidx = reinterpret_cast<const int*>(w + pl.off_sidx);
+    p.sp = reinterpret_cast<const float*>(w + pl.off_sp);
+    p.S = reinterpret_cast<const float*>(w + pl.off_S);
+    p.pm = reinterpret_cast<float*>(w + pl.off_pm);
+    p.pl = reinterpret_cast<float*>(w + pl.off_pl);
+    p.pc = reinterpret_cast<float*>(w + pl.off_pc);
+    p.ld_part = pl.rows_alloc;
+    if ((st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_STATS>(KIND_FWD_LOGITS, di, p, s, "fwd_logits_lse")))
+      return st;
+    const int cblocks = static_cast<int>(cdiv(rows, 32));
+    if ((st = launch(KIND_FWD_COMBINE, s, "fwd_combine", [&] {
+           combine_kernel<<<cblocks, 256, 0, s>>>(p.pm, p.pl, p.pc, pl.rows_alloc, pl.tiles_v, rows, p.S,
+                                                  reinterpret_cast<const float*>(w + pl.off_T), lse + r0,
+                                                  row_loss + r0);
+         })))
+      return st;
+  }
+  if ((st = launch(KIND_LOSS_REDUCE, s, "loss_reduce",
+                   [&] { loss_reduce_kernel<<<1, 1024, 0, s>>>(row_loss, N, loss); })))
+    return st;
+  e = cudaMemcpyAsync(status, dstatus, sizeof(unsigned), cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) {
+    set_error("cudaMemcpyAsync(status)", e);
+    return FCKL_ERR_CUDA;
+  }
+  return FCKL_OK;
+}

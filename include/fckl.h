@@ -87,6 +87,41 @@ int fckl_backward(const void* H, const void* W, int dtype,
                   float grad_scale, void* dH, float* dW,
                   void* ws, size_t ws_bytes, void* stream);
 
+/* Largest device scratch (bytes) that fckl_forward_static can use. The library reserves this
+ * much device memory on every GPU where it is loaded, and keeps it until the process exits. */
+#define FCKL_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* Forward pass that allocates nothing and takes no workspace.
+ *
+ * The pages have no counterpart to this call: it is an interface addition. It serves callers
+ * that cannot allocate device memory at the point of the call, such as a custom operator or
+ * plugin hosted by a framework or inference server that owns all device memory through its
+ * own pool (a raw cudaMalloc there bypasses the pool and may fail once the pool holds the
+ * memory), or a step loop where cudaMalloc/cudaFree and their synchronisation are not
+ * acceptable. Such callers cannot hand fckl_forward a workspace, so this call uses a scratch
+ * array of FCKL_STATIC_SCRATCH_BYTES that the library itself keeps in device memory.
+ *
+ * Inputs and outputs are those of fckl_forward (bf16 H and W only; dtype must be FCKL_BF16),
+ * except that row_loss is required (the loss sum reads it) and
+ *   status : device uint32 [1] <- status bits found on the device by this call
+ *            (0 = clean, bit 0 = a teacher id outside [0, V), bit 1 = a device wait ran out)
+ * The scratch needed is about (8*K + 8 + 12*ceil(V/256)) bytes per row of a chunk rounded up to
+ * 128 rows; a shape above FCKL_STATIC_SCRATCH_BYTES is rejected with FCKL_ERR_WORKSPACE and a
+ * message in fckl_last_error(), before anything is launched. At K = 100 and V = 128256 a chunk
+ * of up to 4096 positions fits.
+ *
+ * The first call on a device looks up the device address of the array (cudaGetSymbolAddress
+ * with that device current) and caches it; make that first call before any stream capture.
+ * Every call on a device shares the one array, which keeps the previous call's contents (the
+ * call clears the status word it needs zeroed): calls whose work overlaps on the GPU (on
+ * different streams, or from different threads) race on it and must be serialised by the
+ * caller. The call calls no cudaMalloc, cudaFree or other allocating routine. */
+int fckl_forward_static(const void* H, const void* W, int dtype,
+                        const int32_t* idx, const float* logp,
+                        int64_t N, int d, int V, int K, int chunk,
+                        float* loss, float* lse, float* row_loss,
+                        uint32_t* status, void* stream);
+
 /* Synchronises `stream`, returns the status found on the device by the last call that
  * used `ws` (FCKL_OK if none), and clears it. */
 int fckl_check(void* ws, void* stream);
