@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--positions", type=int, default=0,
+                    help="run only the first P positions of the workload (profiling, memory sweeps)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -225,6 +227,23 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(value, device=None):
+    """The largest of every rank's value (the slowest rank's time); the value itself on one
+    process. Works with the nccl (CUDA tensors) and gloo (CPU tensors) backends."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(seed, rank):
+    """Each rank runs its own replica of the workload on its own seeded inputs."""
+    return seed + 1000 * rank
+
+
 def run_ours(args):
     import torch
     import chunked_kl_loss_gb300 as fckl
@@ -237,7 +256,7 @@ def run_ours(args):
     dev = torch.device("cuda", local_rank)
     fckl.load()
     w = synthetic.WORKLOADS[args.workload]
-    x = synthetic.make_inputs(w.N, w.d, w.V, w.K, dtype="f32", seed=args.seed + 1000 * rank)
+    x = synthetic.make_inputs(w.N, w.d, w.V, w.K, dtype="f32", seed=replica_seed(args.seed, rank))
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     host = {
         "H": torch.from_numpy(x["H"]).to(tdt).pin_memory(),
@@ -291,12 +310,7 @@ def run_ours(args):
     fckl.check(ws)
     peak_bytes = torch.cuda.max_memory_allocated(dev) - base_alloc
 
-    t_max = elapsed_ms
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
+    t_max = max_over_ranks(elapsed_ms, dev)
 
     # end to end through the public API from pinned host buffers
     e2e = None
@@ -317,12 +331,7 @@ def run_ours(args):
             e2e_step()
         f1.record(stream)
         barrier()
-        e2e_ms = f0.elapsed_time(f1)
-        if world > 1:
-            import torch.distributed as dist
-            tt = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
+        e2e_ms = max_over_ranks(f0.elapsed_time(f1), dev)
         h2d = sum(host[k].numel() * host[k].element_size() for k in host)
         e2e = {"value": world * w.N * args.steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": 4, "ms_per_step": e2e_ms / args.steps}
@@ -376,6 +385,10 @@ def run_ours(args):
 
 def main():
     args = parse()
+    if args.positions:
+        import dataclasses
+        w = synthetic.WORKLOADS[args.workload]
+        synthetic.WORKLOADS[args.workload] = dataclasses.replace(w, N=min(args.positions, w.N))
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
