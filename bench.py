@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--positions", type=int, default=0,
                     help="run only the first P positions of the workload (profiling, memory sweeps)")
+    ap.add_argument("--memory-sweep", action="store_true",
+                    help="peak device memory of one forward+backward at N = W.N/8, W.N/4, W.N/2, W.N "
+                         "(default workload n262144_d3072_v128256), with a linear fit")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -383,8 +386,59 @@ def run_ours(args):
     return 0
 
 
+def bytes_per_position(w):
+    """Device bytes that scale with N: H and dH (d bf16 each), the cache (K int32 + K fp32),
+    lse (fp32) and the per-position loss kept in the workspace (fp32)."""
+    return 2 * w.d + 2 * w.d + 8 * w.K + 4 + 4
+
+
+def memory_sweep(args):
+    """Peak device memory of one forward + backward for growing N at a fixed chunk."""
+    import torch
+    import chunked_kl_loss_gb300 as fckl
+    fckl.load()
+    w = synthetic.WORKLOADS[args.workload]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    x = synthetic.make_inputs(w.N, w.d, w.V, w.K, dtype="f32", seed=args.seed)
+    Hh = torch.from_numpy(x["H"]).to(torch.bfloat16)
+    W = torch.from_numpy(x["W"]).to(dev).to(torch.bfloat16)
+    idx_h, logp_h = torch.from_numpy(x["idx"]), torch.from_numpy(x["logp"])
+    del x
+    points = []
+    for n in (w.N // 8, w.N // 4, w.N // 2, w.N):
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        base = torch.cuda.memory_allocated(dev)  # W already resident
+        torch.cuda.reset_peak_memory_stats(dev)
+        H = Hh[:n].to(dev)
+        idx, logp = idx_h[:n].to(dev), logp_h[:n].to(dev)
+        ws = fckl.Workspace(n, w.d, w.V, w.K, w.chunk, fckl.BF16, dev)
+        loss, lse = fckl.forward(H, W, idx, logp, w.chunk, ws=ws)
+        dH, dW = fckl.backward(H, W, idx, logp, lse, w.chunk, ws=ws)
+        fckl.check(ws)
+        peak = torch.cuda.max_memory_allocated(dev) - base + W.numel() * 2
+        points.append((n, peak))
+        del H, idx, logp, ws, loss, lse, dH, dW
+    n_arr = np.array([p[0] for p in points], dtype=np.float64)
+    y = np.array([p[1] for p in points], dtype=np.float64)
+    b, a = np.polyfit(n_arr, y, 1)
+    resid = np.abs(y - (a + b * n_arr)) / y
+    line = {"metric": "peak device memory of one forward+backward vs N (GiB)", "workload": w.name,
+            "chunk": w.chunk, "points": [{"N": int(n), "peak_gib": pk / 2**30} for n, pk in points],
+            "fit_intercept_gib": a / 2**30, "fit_bytes_per_position": b,
+            "analytic_bytes_per_position": bytes_per_position(w), "max_rel_residual": float(resid.max())}
+    print(json.dumps(line), flush=True)
+    return line
+
+
 def main():
     args = parse()
+    if args.memory_sweep:
+        if args.workload == DEFAULT_WORKLOAD:
+            args.workload = "n262144_d3072_v128256"
+        memory_sweep(args)
+        return 0
     if args.positions:
         import dataclasses
         w = synthetic.WORKLOADS[args.workload]

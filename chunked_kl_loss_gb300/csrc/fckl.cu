@@ -151,10 +151,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D map over a row-major [dim1][dim0] array with row pitch `pitch_bytes`, 128-byte
-// swizzle, zero fill outside the array.
+// 2-D map over a row-major [dim1][dim0] array with row pitch `pitch_bytes`, zero fill
+// outside the array; 128-byte swizzle unless asked otherwise.
 int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t dim0, uint64_t dim1,
-             uint64_t pitch_bytes, uint32_t box0, uint32_t box1) {
+             uint64_t pitch_bytes, uint32_t box0, uint32_t box1,
+             CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = encode_fn();
   if (!enc) {
     set_error_text("cuTensorMapEncodeTiled entry point not found");
@@ -165,7 +166,7 @@ int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t 
   cuuint32_t box[2] = {box0, box1};
   cuuint32_t es[2] = {1, 1};
   CUresult r = enc(m, dt, 2, const_cast<void*>(base), gdim, gstride, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -188,7 +189,7 @@ int64_t rup(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 struct Plan {
   int64_t N;
   int d, V, K, chunk, dt;
-  int rows_alloc;  // chunk rounded up to the 128-row tile
+  int rows_alloc;  // chunk rounded up to 256 rows (the tile of an SM pair)
   int tiles_v;     // vocabulary tiles of 256
   int ldG;         // row pitch (elements) of the bf16 gradient slab
   int bn_d;        // N-tile of the dH / dW products
@@ -196,12 +197,9 @@ struct Plan {
       off_Hb, off_Wb, total;
 };
 
-int choose_bn(int d) {
-  if (d % 256 == 0) return 256;
-  if (d % 192 == 0) return 192;
-  if (d % 128 == 0) return 128;
-  return 256;
-}
+// N-tile of the dH and dW products (over d). 256 columns: an SM pair stages 128 each, two
+// 64-wide swizzle blocks; a d that is not a multiple of 256 ends in a ragged tile.
+int choose_bn(int) { return 256; }
 
 int check_shape(int64_t N, int d, int V, int K, int chunk, int dt) {
   if (N < 1 || d < 1 || V < 1 || K < 1 || chunk < 1) return FCKL_ERR_ARG;
@@ -220,7 +218,7 @@ Plan make_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
   p.K = K;
   p.chunk = static_cast<int>(std::min<int64_t>(chunk, N));
   p.dt = dt;
-  p.rows_alloc = static_cast<int>(rup(p.chunk, BM));
+  p.rows_alloc = static_cast<int>(rup(p.chunk, 256));
   p.tiles_v = static_cast<int>(cdiv(V, VOCAB_TILE));
   p.ldG = static_cast<int>(rup(V, 8));
   p.bn_d = choose_bn(d);
@@ -251,32 +249,52 @@ Plan make_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // ------------------------------------------------------------------ kernel launchers
+#ifndef FCKL_CG
+#define FCKL_CG 2  // CTAs per MMA in the four products: 2 = SM pairs (cta_group::2)
+#endif
+constexpr int CG = FCKL_CG;
+constexpr int TILE_M = BM * CG;  // rows of one MMA tile
+
+// Persistent launch: one CTA (pair) per SM (pair), as many as can be resident, capped by the
+// number of work units.
 template <int BN, bool AMN, bool BMN, int EPI>
 int launch_tc(int kind, DevInfo* di, const TcParams& p, cudaStream_t s, const char* what) {
-  auto k = tc_gemm_kernel<BN, AMN, BMN, EPI>;
-  constexpr uint32_t smem = TcSmem<BN>::DYN_BYTES;
+  auto k = tc_gemm_kernel<CG, BN, AMN, BMN, EPI>;
+  constexpr uint32_t smem = TcSmem<CG, BN>::DYN_BYTES;
   static_assert(smem <= 232448, "shared memory budget");
   static bool attr_done[64] = {};  // one flag per device for this instantiation
+  static int max_clusters[64] = {};
   const int dev = di->id;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = CG > 1 ? 1 : 0;
   if (!attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) {
       set_error("cudaFuncSetAttribute", e);
       return FCKL_ERR_CUDA;
     }
+    int n = di->sms / CG;
+    if (CG > 1) {
+      cfg.gridDim = dim3(static_cast<unsigned>(CG * n));
+      int m = 0;
+      if (cudaOccupancyMaxActiveClusters(&m, k, &cfg) == cudaSuccess && m > 0) n = std::min(n, m);
+      cudaGetLastError();
+    }
+    max_clusters[dev] = n;
     attr_done[dev] = true;
   }
-  const int grid = static_cast<int>(std::min<int64_t>(p.num_units, di->sms));
-  return launch(kind, s, what, [&] { k<<<grid, NUM_THREADS, smem, s>>>(p); });
-}
-
-template <bool AMN, bool BMN, int EPI>
-int launch_tc_bn(int bn, int kind, DevInfo* di, const TcParams& p, cudaStream_t s, const char* what) {
-  switch (bn) {
-    case 256: return launch_tc<256, AMN, BMN, EPI>(kind, di, p, s, what);
-    case 192: return launch_tc<192, AMN, BMN, EPI>(kind, di, p, s, what);
-    default: return launch_tc<128, AMN, BMN, EPI>(kind, di, p, s, what);
-  }
+  const int clusters = static_cast<int>(std::min<int64_t>(p.num_units, max_clusters[dev]));
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG));
+  return launch(kind, s, what, [&] { cudaLaunchKernelEx(&cfg, k, p); });
 }
 
 int launch_cvt(const float* src, void* dst, int64_t n, DevInfo* di, cudaStream_t s) {
@@ -355,7 +373,7 @@ int fckl_forward(const void* H, const void* W, int dtype, const int32_t* idx, co
     Wb = w + pl.off_Wb;
   }
   CUtensorMap tmW;
-  if ((st = make_map(&tmW, Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK, VOCAB_TILE))) return st;
+  if ((st = make_map(&tmW, Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK, VOCAB_TILE / CG))) return st;
   const size_t esz = dtype == FCKL_F32 ? 4 : 2;
   for (int64_t r0 = 0; r0 < N; r0 += pl.chunk) {
     const int rows = static_cast<int>(std::min<int64_t>(pl.chunk, N - r0));
@@ -369,7 +387,7 @@ int fckl_forward(const void* H, const void* W, int dtype, const int32_t* idx, co
     memset(&p, 0, sizeof(p));
     if ((st = make_map(&p.tmA, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM))) return st;
     p.tmB = tmW;
-    p.sch = {static_cast<int>(cdiv(rows, BM)), pl.tiles_v, static_cast<int>(cdiv(d, BK)), 1,
+    p.sch = {static_cast<int>(cdiv(rows, TILE_M)), pl.tiles_v, static_cast<int>(cdiv(d, BK)), 1,
              static_cast<int>(cdiv(d, BK)), 1};
     p.num_units = p.sch.m_blocks * p.sch.n_blocks;
     p.status = status;
@@ -419,10 +437,13 @@ int fckl_backward(const void* H, const void* W, int dtype, const int32_t* idx, c
     Wb = w + pl.off_Wb;
   }
   const int bn = pl.bn_d;
-  CUtensorMap tmW_k, tmW_mn, tmDW;
-  if ((st = make_map(&tmW_k, Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK, VOCAB_TILE))) return st;
+  CUtensorMap tmW_k, tmW_mn, tmDW, tmDWp;
+  if ((st = make_map(&tmW_k, Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK, VOCAB_TILE / CG))) return st;
   if ((st = make_map(&tmW_mn, Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, 64, BK))) return st;
   if ((st = make_map(&tmDW, dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, V, uint64_t(d) * 4, 32, 32))) return st;
+  if ((st = make_map(&tmDWp, dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, V, uint64_t(d) * 4, 256, BM,
+                     CU_TENSOR_MAP_SWIZZLE_NONE)))
+    return st;
   void* G = w + pl.off_G;
   float* dhp = reinterpret_cast<float*>(w + pl.off_dhp);
   const size_t esz = dtype == FCKL_F32 ? 4 : 2;
@@ -430,7 +451,7 @@ int fckl_backward(const void* H, const void* W, int dtype, const int32_t* idx, c
 
   for (int64_t r0 = 0; r0 < N; r0 += pl.chunk) {
     const int rows = static_cast<int>(std::min<int64_t>(pl.chunk, N - r0));
-    const int mbr = static_cast<int>(cdiv(rows, BM));
+    const int mbr = static_cast<int>(cdiv(rows, TILE_M));
     if ((st = launch_preprocess(pl, idx + r0 * K, logp + r0 * K, rows, w, status, di, s))) return st;
     const void* Hc = static_cast<const uint8_t*>(H) + static_cast<size_t>(r0) * d * esz;
     if (dtype == FCKL_F32) {
@@ -470,7 +491,8 @@ int fckl_backward(const void* H, const void* W, int dtype, const int32_t* idx, c
         const int kbps = static_cast<int>(cdiv(kb_v, sp));
         if (cdiv(kb_v, kbps) != sp) continue;
         const int64_t units = int64_t(tiles) * sp;
-        const double eff = double(units) / double(cdiv(units, di->sms) * di->sms);
+        const int64_t slots = di->sms / CG;
+        const double eff = double(units) / double(cdiv(units, slots) * slots);
         if (eff > best + 0.02) {
           best = eff;
           splits = sp;
@@ -493,7 +515,7 @@ int fckl_backward(const void* H, const void* W, int dtype, const int32_t* idx, c
     ph.c_reduce = 0;
     ph.c_xlim = d;
     ph.c_ylim = splits * pl.rows_alloc;
-    if ((st = launch_tc_bn<false, true, EPI_STORE_F32>(bn, KIND_BWD_DH, di, ph, s, "bwd_dH_gemm"))) return st;
+    if ((st = launch_tc<256, false, true, EPI_STORE_F32>(KIND_BWD_DH, di, ph, s, "bwd_dH_gemm"))) return st;
     {
       const int64_t n4 = int64_t(rows) * d / 4;
       const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(n4, 256), int64_t(di->sms) * 8)));
@@ -518,15 +540,17 @@ int fckl_backward(const void* H, const void* W, int dtype, const int32_t* idx, c
       return st;
     if ((st = make_map(&pw.tmB, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, 64, BK))) return st;
     pw.tmC = tmDW;
+    pw.tmP = tmDWp;
     const int kb_r = static_cast<int>(cdiv(rows, BK));
-    pw.sch = {static_cast<int>(cdiv(V, BM)), nbd, kb_r, 1, kb_r, 0};
+    pw.sch = {static_cast<int>(cdiv(V, TILE_M)), nbd, kb_r, 1, kb_r, 0};
     pw.num_units = pw.sch.m_blocks * nbd;
     pw.status = status;
     pw.c_split_rows = 0;
     pw.c_reduce = r0 > 0 ? 1 : 0;
+    pw.c_prefetch = pw.c_reduce;
     pw.c_xlim = d;
     pw.c_ylim = V;
-    if ((st = launch_tc_bn<true, true, EPI_STORE_F32>(bn, KIND_BWD_DW, di, pw, s, "bwd_dW_gemm"))) return st;
+    if ((st = launch_tc<256, true, true, EPI_STORE_F32>(KIND_BWD_DW, di, pw, s, "bwd_dW_gemm"))) return st;
   }
   return FCKL_OK;
 }
@@ -692,7 +716,7 @@ extern "C" int fckl_forward_static(const void* H, const void* W, int dtype, cons
     return FCKL_ERR_CUDA;
   }
   CUtensorMap tmW;
-  if ((st = make_map(&tmW, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK, VOCAB_TILE))) return st;
+  if ((st = make_map(&tmW, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK, VOCAB_TILE / CG))) return st;
   for (int64_t r0 = 0; r0 < N; r0 += pl.chunk) {
     const int rows = static_cast<int>(std::min<int64_t>(pl.chunk, N - r0));
     if ((st = launch_preprocess(pl, idx + r0 * K, logp + r0 * K, rows, w, dstatus, di, s))) return st;
@@ -701,7 +725,7 @@ extern "C" int fckl_forward_static(const void* H, const void* W, int dtype, cons
     memset(&p, 0, sizeof(p));
     if ((st = make_map(&p.tmA, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM))) return st;
     p.tmB = tmW;
-    p.sch = {static_cast<int>(cdiv(rows, BM)), pl.tiles_v, static_cast<int>(cdiv(d, BK)), 1,
+    p.sch = {static_cast<int>(cdiv(rows, TILE_M)), pl.tiles_v, static_cast<int>(cdiv(d, BK)), 1,
              static_cast<int>(cdiv(d, BK)), 1};
     p.num_units = p.sch.m_blocks * p.sch.n_blocks;
     p.status = dstatus;

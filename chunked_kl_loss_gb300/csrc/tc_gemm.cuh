@@ -1,9 +1,13 @@
 // Persistent, warp-specialised tcgen05 GEMM engine for the fused chunked KL loss.
 //
-// One CTA per SM (1-CTA MMA, 128 x BN tiles, K-blocks of 64 bf16), 192 threads:
-//   warp 0     : TMA producer (one lane) filling a STAGES-deep shared-memory ring
-//   warp 1     : TMEM owner and MMA issuer (one lane); two TMEM accumulators of 128 x 256
-//                fp32 so the epilogue of one tile overlaps the main loop of the next
+// One CTA per SM, 192 threads. With CG = 2 two SMs of a cluster form a pair that computes a
+// 256 x BN tile with tcgen05.mma.cta_group::2: each CTA stages its 128 rows of A and half of
+// B, the even CTA issues the MMAs, and each CTA's TMEM receives its 128 rows of the result
+// (CG = 1: one CTA per 128 x BN tile). K-blocks of 64 bf16.
+//   warp 0     : TMA producer (one lane) filling a shared-memory ring (6 stages for pairs)
+//   warp 1     : TMEM owner and, in the even CTA, MMA issuer (one lane); two TMEM
+//                accumulators of 128 x 256 fp32 per CTA so the epilogue of one tile
+//                overlaps the main loop of the next
 //   warps 2..5 : epilogue, one TMEM lane quarter (32 rows) each
 // Work units (tile, K-split) are dealt round-robin over the persistent CTAs in an order
 // chosen by the host so that concurrently running CTAs share operand tiles in L2.
@@ -28,9 +32,8 @@
 
 namespace fckl {
 
-constexpr int BM = 128;
-constexpr int BK = 64;
-constexpr int STAGES = 4;
+constexpr int BM = 128;  // rows of A per CTA
+constexpr int BK = 64;   // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int EPI_WARPS = 4;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
@@ -52,6 +55,7 @@ struct TcParams {
   CUtensorMap tmA;  // operand A (M x K)
   CUtensorMap tmB;  // operand B (N x K)
   CUtensorMap tmC;  // epilogue output
+  CUtensorMap tmP;  // epilogue output, unswizzled 128-row x 256-column boxes for L2 prefetch
   Sched sch;
   int num_units;
   unsigned* status;
@@ -70,12 +74,17 @@ struct TcParams {
   int c_split_rows;  // rows between the slabs of successive K-splits in tmC
   int c_reduce;      // 1: reduce-add into tmC, 0: plain store
   int c_xlim, c_ylim;  // extent of tmC: boxes starting at or past it are not issued
+  int c_prefetch;      // 1: prefetch each unit's output tile into L2 when its loads start
 };
 
-template <int BN>
+// Shared-memory layout of one CTA. CG = CTAs per MMA (1: a 128 x BN tile per CTA; 2: a
+// 256 x BN tile per CTA pair, each CTA holding its 128 rows of A and BN/2 rows of B).
+template <int CG, int BN>
 struct TcSmem {
+  static constexpr int STAGES = CG == 2 ? 6 : 4;
+  static constexpr int BN_CTA = BN / CG;
   static constexpr uint32_t A_BYTES = BM * BK * 2;
-  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t B_BYTES = BN_CTA * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t EPI_OFF = STAGES * STAGE_BYTES;
   static constexpr uint32_t BAR_OFF = EPI_OFF + EPI_WARPS * 2 * EPI_BUF_BYTES;
@@ -170,14 +179,36 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI>
+// Bounded wait whose acquire also covers arrivals from the peer CTA of a pair.
+__device__ __forceinline__ bool wait_phase_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                   unsigned* status) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 31u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > WAIT_TIMEOUT_NS) {
+        *abort_flag = 1;
+        atomicOr(status, ST_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+template <int CG, int BN, bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-  using L = TcSmem<BN>;
+  using L = TcSmem<CG, BN>;
+  constexpr int NST = L::STAGES;
+  constexpr int BN_CTA = L::BN_CTA;
+  static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per MMA");
+  static_assert(!B_MN || BN_CTA % 64 == 0, "MN-major B is staged in 64-wide blocks");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-  uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
+  uint64_t* empty = full + NST;
+  uint64_t* tfull = empty + NST;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
@@ -185,15 +216,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;  // position in the CTA pair
+  const bool leader = rank == 0;
+  const int cluster_id = blockIdx.x / CG;
+  const int num_clusters = gridDim.x / CG;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], EPI_WARPS);
+      mbar_init(&tempty[a], EPI_WARPS * CG);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -203,67 +238,99 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     if (EPI != EPI_FWD_STATS) prefetch_tmap(&p.tmC);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (CG == 2) {
+      tmem_alloc_pair(tmem_holder, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_holder, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // the peer's barriers exist before anyone signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer (each CTA)
     if (lane == 0) {
       uint32_t cnt = 0;
       uint32_t armed = 0, armed_par = 0;  // per stage: ever armed, parity of the last arming
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+      const uint32_t full_base = CG == 2 ? mapa_shared(smem_u32(full), 0) : smem_u32(full);
+      for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
         int mb, nb, sp, kb0, kb1;
         decode_unit(p.sch, u, mb, nb, sp, kb0, kb1);
+        const int arow = mb * BM * CG + static_cast<int>(rank) * BM;       // this CTA's A rows
+        const int bcol = nb * BN + static_cast<int>(rank) * BN_CTA;        // this CTA's B rows/cols
+        // A reduce-add epilogue reads its output tile back from memory: start that read now,
+        // a whole main loop before the epilogue needs it.
+        if (EPI == EPI_STORE_F32 && p.c_prefetch && nb * BN < p.c_xlim && arow < p.c_ylim)
+          tma_prefetch_l2_2d(&p.tmP, nb * BN, arow);
         for (int kb = kb0; kb < kb1; ++kb, ++cnt) {
-          const uint32_t s = cnt % STAGES, ph = (cnt / STAGES) & 1u;
+          const uint32_t s = cnt % NST, ph = (cnt / NST) & 1u;
           if (!wait_phase(&empty[s], ph ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES);
-          armed |= 1u << s;
-          armed_par = (armed_par & ~(1u << s)) | (ph << s);
+          if (leader) {
+            mbar_arrive_expect_tx(&full[s], CG * L::STAGE_BYTES);
+            armed |= 1u << s;
+            armed_par = (armed_par & ~(1u << s)) | (ph << s);
+          }
           uint8_t* a = smem + s * L::STAGE_BYTES;
           uint8_t* b = a + L::A_BYTES;
+          const uint32_t fb = full_base + s * 8u;
+          auto load = [&](void* dst, const CUtensorMap* m, int x, int y) {
+            if constexpr (CG == 2)
+              tma_load_2d_pair(dst, m, fb, x, y);
+            else
+              tma_load_2d(dst, m, &full[s], x, y);
+          };
           if (!A_MN) {
-            tma_load_2d(a, &p.tmA, &full[s], kb * BK, mb * BM);
+            load(a, &p.tmA, kb * BK, arow);
           } else {
 #pragma unroll
-            for (int j = 0; j < BM / 64; ++j) tma_load_2d(a + j * 8192, &p.tmA, &full[s], mb * BM + 64 * j, kb * BK);
+            for (int j = 0; j < BM / 64; ++j) load(a + j * 8192, &p.tmA, arow + 64 * j, kb * BK);
           }
           if (!B_MN) {
-            tma_load_2d(b, &p.tmB, &full[s], kb * BK, nb * BN);
+            load(b, &p.tmB, kb * BK, bcol);
           } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_2d(b + j * 8192, &p.tmB, &full[s], nb * BN + 64 * j, kb * BK);
+            for (int j = 0; j < BN_CTA / 64; ++j) load(b + j * 8192, &p.tmB, bcol + 64 * j, kb * BK);
           }
         }
       }
-      // Every copy this thread started must land before the CTA may exit.
-      for (int s = 0; s < STAGES; ++s)
-        if (armed & (1u << s)) drain_phase(&full[s], (armed_par >> s) & 1u, p.status);
+      // Every copy this pair started must land before a CTA may exit. The leader's full
+      // barriers count both CTAs' bytes; a peer that gave up early waits a little for its
+      // own copies, whose barrier it cannot poll.
+      if (leader) {
+        for (int s = 0; s < NST; ++s)
+          if (armed & (1u << s)) drain_phase(&full[s], (armed_par >> s) & 1u, p.status);
+      } else if (!ok) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
+      }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, A_MN, B_MN);
+    // ------------------------------------------------------------ MMA issuer (leader CTA)
+    if (lane == 0 && leader) {
+      constexpr uint32_t IDESC = make_idesc_bf16(BM * CG, BN, A_MN, B_MN);
       uint32_t cnt = 0, it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+      for (int u = cluster_id; ok && u < p.num_units; u += num_clusters, ++it) {
         int mb, nb, sp, kb0, kb1;
         decode_unit(p.sch, u, mb, nb, sp, kb0, kb1);
         const uint32_t acc = it & 1u, use = it >> 1;
-        if (!wait_phase(&tempty[acc], (use & 1u) ^ 1u, abort_flag, p.status)) break;
+        const bool got = CG == 2 ? wait_phase_cluster(&tempty[acc], (use & 1u) ^ 1u, abort_flag, p.status)
+                                 : wait_phase(&tempty[acc], (use & 1u) ^ 1u, abort_flag, p.status);
+        if (!got) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
         for (int kb = kb0; kb < kb1; ++kb, ++cnt) {
-          const uint32_t s = cnt % STAGES, ph = (cnt / STAGES) & 1u;
+          const uint32_t s = cnt % NST, ph = (cnt / NST) & 1u;
           if (!wait_phase(&full[s], ph, abort_flag, p.status)) {
             ok = false;
             break;
@@ -277,28 +344,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                                      : make_sdesc_sw128(a_addr + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? make_sdesc_sw128(b_addr + kk * 2048, 8192, 1024)
                                      : make_sdesc_sw128(b_addr + kk * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+            if constexpr (CG == 2)
+              umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+            else
+              umma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&empty[s]);
+          if constexpr (CG == 2)
+            umma_commit_pair(&empty[s], 0x3);
+          else
+            umma_commit(&empty[s]);
         }
         if (!ok) break;
-        umma_commit(&tfull[acc]);
+        if constexpr (CG == 2)
+          umma_commit_pair(&tfull[acc], 0x3);
+        else
+          umma_commit(&tfull[acc]);
       }
       // All MMAs issued by this thread must finish before TMEM is released.
-      umma_commit(drain);
+      if constexpr (CG == 2)
+        umma_commit_pair(drain, 0x1);
+      else
+        umma_commit(drain);
       drain_phase(drain, 0, p.status);
     }
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (each CTA)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     uint8_t* ebuf0 = smem + L::EPI_OFF + (warp - 2) * 2 * EPI_BUF_BYTES;
+    const uint32_t tempty_leader = CG == 2 ? mapa_shared(smem_u32(tempty), 0) : 0u;
+    auto release_acc = [&](uint32_t acc) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (CG == 2 && !leader)
+          mbar_arrive_cluster(tempty_leader + acc * 8u);
+        else
+          mbar_arrive(&tempty[acc]);
+      }
+    };
     uint32_t it = 0, ecnt = 0;
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
+    for (int u = cluster_id; u < p.num_units; u += num_clusters, ++it) {
       int mb, nb, sp, kb0, kb1;
       decode_unit(p.sch, u, mb, nb, sp, kb0, kb1);
       const uint32_t acc = it & 1u, use = it >> 1;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * ACC_STRIDE;
-      const int row = mb * BM + 32 * q + lane;
+      const int row0 = mb * BM * CG + static_cast<int>(rank) * BM + 32 * q;  // first row of this warp
+      const int row = row0 + lane;
 
       if constexpr (EPI == EPI_FWD_STATS || EPI == EPI_LOGIT_GRAD) {
         const bool valid = row < p.rows_valid;
@@ -319,11 +410,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             float x[32];
             __syncwarp();
             tmem_ld32(taddr + 32 * j, x);
-            if (j == BN / 32 - 1) {
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&tempty[acc]);
-            }
+            if (j == BN / 32 - 1) release_acc(acc);
             const int cb = v0 + 32 * j;
             if (cb + 32 > p.V) {
 #pragma unroll
@@ -368,11 +455,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
               float x[32];
               __syncwarp();
               tmem_ld32(taddr + 32 * j, x);
-              if (j == BN / 32 - 1) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[acc]);
-              }
+              if (j == BN / 32 - 1) release_acc(acc);
               const int cb = v0 + 32 * j;
 #pragma unroll
               for (int t = 0; t < 32; ++t) x[t] = a * ex2_approx(fmaf(x[t], LOG2E, nl));
@@ -395,8 +478,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              const int sx = v0 + 64 * jj, sy = mb * BM + 32 * q;
-              if (sx < p.c_xlim && sy < p.c_ylim) tma_store_2d(&p.tmC, buf, sx, sy);
+              const int sx = v0 + 64 * jj;
+              if (sx < p.c_xlim && row0 < p.c_ylim) tma_store_2d(&p.tmC, buf, sx, row0);
               bulk_commit();
             }
           }
@@ -405,7 +488,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         // EPI_STORE_F32
         if (!warp_wait_phase(&tfull[acc], use & 1u, abort_flag, p.status)) break;
         tc_fence_after();
-        const int y = sp * p.c_split_rows + mb * BM + 32 * q;
+        const int y = sp * p.c_split_rows + row0;
 #pragma unroll 1
         for (int j = 0; j < BN / 32; ++j, ++ecnt) {
           uint8_t* buf = ebuf0 + (ecnt & 1u) * EPI_BUF_BYTES;
@@ -413,11 +496,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           __syncwarp();
           float x[32];
           tmem_ld32(taddr + 32 * j, x);
-          if (j == BN / 32 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
-          }
+          if (j == BN / 32 - 1) release_acc(acc);
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) {
             const int chunk16 = cc ^ (lane & 7);
@@ -445,9 +524,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // the leader's MMAs into this CTA's TMEM are done
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (CG == 2)
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 

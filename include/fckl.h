@@ -106,7 +106,7 @@ int fckl_backward(const void* H, const void* W, int dtype,
  *   status : device uint32 [1] <- status bits found on the device by this call
  *            (0 = clean, bit 0 = a teacher id outside [0, V), bit 1 = a device wait ran out)
  * The scratch needed is about (8*K + 8 + 12*ceil(V/256)) bytes per row of a chunk rounded up to
- * 128 rows; a shape above FCKL_STATIC_SCRATCH_BYTES is rejected with FCKL_ERR_WORKSPACE and a
+ * 256 rows; a shape above FCKL_STATIC_SCRATCH_BYTES is rejected with FCKL_ERR_WORKSPACE and a
  * message in fckl_last_error(), before anything is launched. At K = 100 and V = 128256 a chunk
  * of up to 4096 positions fits.
  *
