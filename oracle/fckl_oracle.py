@@ -33,6 +33,10 @@ with 0 * log 0 taken as 0 (an entry whose logp is -inf adds nothing). Each
 cache slot is its own term: a token id repeated within a row contributes once
 per slot. The loss is a SUM over positions; a caller divides for a mean.
 
+Optional position weights w_n (default 1) make the loss sum_n w_n loss_n: a
+weight of 0 drops a padded position, the plain reading of the sequence packing
+the article lists among its ablations (same page, section "得到的 student").
+
 Differentiating, with p_sparse_nv = sum_{k: idx_nk = v} p_nk,
 
     G_nv  = d loss / d z_nv = S_n softmax(z_n)_v - p_sparse_nv
@@ -110,14 +114,25 @@ def _check(H, W, idx, logp):
         raise IndexError("teacher index outside [0, V)")
 
 
-def forward(H, W, idx, logp, chunk=None):
-    """Loss (sum over positions), lse [N] and per-position loss [N], chunk by chunk.
+def _weights(weight, N):
+    if weight is None:
+        return np.ones(N)
+    w = np.asarray(weight, dtype=np.float64)
+    if w.shape != (N,):
+        raise ValueError("weight must be [N]")
+    return w
+
+
+def forward(H, W, idx, logp, chunk=None, weight=None):
+    """Loss (weighted sum over positions), lse [N] and per-position weighted loss [N],
+    chunk by chunk.
 
     "Fused, chunked KL loss": each chunk's logits are formed, folded into the
     accumulated loss and dropped before the next chunk.
     """
     _check(H, W, idx, logp)
     N = np.shape(H)[0]
+    w = _weights(weight, N)
     chunk = N if not chunk else int(chunk)
     lse = np.empty(N)
     rl = np.empty(N)
@@ -125,11 +140,11 @@ def forward(H, W, idx, logp, chunk=None):
         e = min(N, s + chunk)
         z = logits(H[s:e], W)
         lse[s:e] = log_partition(z)
-        rl[s:e] = row_loss(z, lse[s:e], idx[s:e], logp[s:e])
+        rl[s:e] = w[s:e] * row_loss(z, lse[s:e], idx[s:e], logp[s:e])
     return float(rl.sum()), lse, rl
 
 
-def backward(H, W, idx, logp, grad_scale=1.0, chunk=None):
+def backward(H, W, idx, logp, grad_scale=1.0, chunk=None, weight=None):
     """dH [N,d] and dW [V,d] (fp64), each chunk's logits recomputed.
 
     "Fused, chunked KL loss": the backward pass recomputes each chunk instead of
@@ -138,6 +153,7 @@ def backward(H, W, idx, logp, grad_scale=1.0, chunk=None):
     """
     _check(H, W, idx, logp)
     N, d = np.shape(H)
+    w = _weights(weight, N)
     W64 = np.asarray(W, dtype=np.float64)
     chunk = N if not chunk else int(chunk)
     dH = np.empty((N, d))
@@ -147,30 +163,31 @@ def backward(H, W, idx, logp, grad_scale=1.0, chunk=None):
         H64 = np.asarray(H[s:e], dtype=np.float64)
         z = H64 @ W64.T
         lse = log_partition(z)
-        G = logit_grad(z, lse, idx[s:e], logp[s:e]) * grad_scale
+        G = logit_grad(z, lse, idx[s:e], logp[s:e]) * (grad_scale * w[s:e])[:, None]
         dH[s:e] = G @ W64
         dW += G.T @ H64
     return dH, dW
 
 
-def forward_backward(H, W, idx, logp, grad_scale=1.0, chunk=None):
+def forward_backward(H, W, idx, logp, grad_scale=1.0, chunk=None, weight=None):
     """(loss, lse, dH, dW) in one pass over the chunks."""
-    loss, lse, _ = forward(H, W, idx, logp, chunk)
-    dH, dW = backward(H, W, idx, logp, grad_scale, chunk)
+    loss, lse, _ = forward(H, W, idx, logp, chunk, weight)
+    dH, dW = backward(H, W, idx, logp, grad_scale, chunk, weight)
     return loss, lse, dH, dW
 
 
-def rows(H, W, idx, logp, which, grad_scale=1.0):
+def rows(H, W, idx, logp, which, grad_scale=1.0, weight=None):
     """lse_n, loss_n and dH_n for selected positions only.
 
     Every one of these depends on its own position alone (its logits row and its
     cache row), so they can be checked one by one at any problem size.
     """
     which = np.asarray(which, dtype=np.int64)
+    w = _weights(weight, np.shape(H)[0])[which]
     Hs = np.asarray(H)[which]
     W64 = np.asarray(W, dtype=np.float64)
     z = np.asarray(Hs, dtype=np.float64) @ W64.T
     lse = log_partition(z)
-    rl = row_loss(z, lse, np.asarray(idx)[which], np.asarray(logp)[which])
-    G = logit_grad(z, lse, np.asarray(idx)[which], np.asarray(logp)[which]) * grad_scale
+    rl = w * row_loss(z, lse, np.asarray(idx)[which], np.asarray(logp)[which])
+    G = logit_grad(z, lse, np.asarray(idx)[which], np.asarray(logp)[which]) * (grad_scale * w)[:, None]
     return lse, rl, G @ W64

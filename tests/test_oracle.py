@@ -261,3 +261,42 @@ def test_golden_fixture():
     np.testing.assert_allclose(lse[:8], g["lse_head"], rtol=1e-12)
     np.testing.assert_allclose(dH[0, :8], g["dH_row0"], rtol=1e-10, atol=1e-14)
     np.testing.assert_allclose(dW[x["idx"][0, 0], :8], g["dW_hit_row"], rtol=1e-10, atol=1e-14)
+
+
+def test_weight_zero_drops_a_position_and_two_duplicates_it():
+    x = _problem(12, 16, 128, 6, seed=14)
+    w = np.ones(12)
+    w[[2, 7]] = 0.0
+    w[5] = 2.0
+    got = orc.forward_backward(x["H"], x["W"], x["idx"], x["logp"], grad_scale=0.5, chunk=5, weight=w)
+    keep = [i for i in range(12) if w[i] != 0] + [5]          # drop 2 and 7, repeat 5
+    ref = orc.forward_backward(x["H"][keep], x["W"], x["idx"][keep], x["logp"][keep], grad_scale=0.5)
+    assert got[0] == pytest.approx(ref[0], rel=1e-12)
+    np.testing.assert_allclose(got[3], ref[3], rtol=1e-11, atol=1e-14)          # dW
+    assert np.abs(got[2][[2, 7]]).max() == 0.0                                  # dropped rows
+    np.testing.assert_allclose(got[2][5], 2 * ref[2][keep.index(5)], rtol=1e-12)
+    np.testing.assert_allclose(got[1], orc.forward(x["H"], x["W"], x["idx"], x["logp"])[1], rtol=1e-14)
+
+
+def test_weighted_finite_differences():
+    rng = np.random.default_rng(15)
+    N, d, V, K = 3, 6, 20, 4
+    H = rng.standard_normal((N, d))
+    W = rng.standard_normal((V, d)) / np.sqrt(d)
+    idx, logp = synthetic.teacher_cache(N, V, K, seed=16)
+    w = np.array([0.3, 0.0, 1.7])
+    dH, dW = orc.backward(H, W, idx, logp, grad_scale=1.0, weight=w)
+    h = 1e-6
+    for _ in range(6):
+        i, j = rng.integers(N), rng.integers(d)
+        Hp, Hm = H.copy(), H.copy()
+        Hp[i, j] += h
+        Hm[i, j] -= h
+        fd = (orc.forward(Hp, W, idx, logp, weight=w)[0] - orc.forward(Hm, W, idx, logp, weight=w)[0]) / (2 * h)
+        assert fd == pytest.approx(dH[i, j], rel=1e-6, abs=1e-9)
+        v, j = rng.integers(V), rng.integers(d)
+        Wp, Wm = W.copy(), W.copy()
+        Wp[v, j] += h
+        Wm[v, j] -= h
+        fd = (orc.forward(H, Wp, idx, logp, weight=w)[0] - orc.forward(H, Wm, idx, logp, weight=w)[0]) / (2 * h)
+        assert fd == pytest.approx(dW[v, j], rel=1e-6, abs=1e-9)
