@@ -116,6 +116,8 @@ class Workspace:
         return ctypes.c_void_p(self.tensor.data_ptr())
 
 
+# Workspace of the last call, for check(): held strongly when the binding created it (the
+# caller has no other handle), weakly when the caller passed it in (the caller owns it).
 _last_ws = None
 
 
@@ -135,9 +137,12 @@ def _shape(H, W, idx, logp):
 
 def _ws_for(ws, N, d, V, K, chunk, dt, device):
     global _last_ws
+    import weakref
     if ws is None:
         ws = Workspace(N, d, V, K, chunk, dt, device)
-    _last_ws = ws
+        _last_ws = ws
+    else:
+        _last_ws = weakref.ref(ws)
     return ws
 
 
@@ -187,7 +192,9 @@ def forward_backward(H, W, idx, logp, chunk, grad_scale=1.0, ws=None, stream=Non
 def check(ws=None, stream=None, raise_on_error=True) -> int:
     """Synchronises and reads the device status word of ``ws`` (default: the workspace
     of the last call); raises FcklError on a device-detected error."""
-    ws = ws if ws is not None else _last_ws
+    if ws is None and _last_ws is not None:
+        import weakref
+        ws = _last_ws() if isinstance(_last_ws, weakref.ref) else _last_ws
     if ws is None:
         return OK
     st = load().fckl_check(ws.ptr, _stream_ptr(stream))
