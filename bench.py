@@ -2,8 +2,9 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-One step = fckl_forward + fckl_backward over the whole workload (all chunks), inputs
-resident in HBM. Prints one JSON line (rank 0). Under torchrun each rank runs its own
+One step = one forward + backward over the whole workload (all chunks), inputs resident in
+HBM: one fckl_forward_backward call (--api fused, the default) or fckl_forward then
+fckl_backward (--api separate). Prints one JSON line (rank 0). Under torchrun each rank runs its own
 replica of the workload (the loss has no exchange step on one GPU: replicas only) and
 the whole-job value is the positions of all ranks over the slowest rank's time.
 
@@ -50,6 +51,8 @@ def parse():
     ap.add_argument("--memory-sweep", action="store_true",
                     help="peak device memory of one forward+backward at N = W.N/8, W.N/4, W.N/2, W.N "
                          "(default workload n262144_d3072_v128256), with a linear fit")
+    ap.add_argument("--api", default="fused", choices=["fused", "separate"],
+                    help="one fckl_forward_backward call per step, or fckl_forward then fckl_backward")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -119,7 +122,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": config_of(w),
+            "config": config_of(w, args.api),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
                              "sample": f"each step: fp64 oracle forward+backward on {n} of {w.N} positions "
                                        f"(full V, d)"},
@@ -128,9 +131,9 @@ def run_reference(args):
     return 0
 
 
-def config_of(w):
+def config_of(w, api="fused"):
     return {"workload": w.name, "N": w.N, "d": w.d, "V": w.V, "K": w.K, "chunk": w.chunk,
-            "input_dtype": w.dtype, "parallelism": "replicas",
+            "input_dtype": w.dtype, "parallelism": "replicas", "api": api,
             "l2": "inputs larger than L2 (W alone is %.0f MB)" % (w.V * w.d * 2 / 1e6)}
 
 
@@ -278,6 +281,9 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     def step():
+        if args.api == "fused":
+            loss, _, _, _ = fckl.forward_backward(H, W, idx, logp, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW)
+            return loss
         loss, lse = fckl.forward(H, W, idx, logp, w.chunk, ws=ws, stream=stream)
         fckl.backward(H, W, idx, logp, lse, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW)
         return loss
@@ -322,8 +328,12 @@ def run_ours(args):
 
         def e2e_step():
             Hd, Wd, idd, lpd = (host[k].to(dev, non_blocking=True) for k in ("H", "W", "idx", "logp"))
-            loss, lse = fckl.forward(Hd, Wd, idd, lpd, w.chunk, ws=ws, stream=stream)
-            fckl.backward(Hd, Wd, idd, lpd, lse, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW)
+            if args.api == "fused":
+                loss, _, _, _ = fckl.forward_backward(Hd, Wd, idd, lpd, w.chunk, ws=ws, stream=stream, dH=dH,
+                                                      dW=dW)
+            else:
+                loss, lse = fckl.forward(Hd, Wd, idd, lpd, w.chunk, ws=ws, stream=stream)
+                fckl.backward(Hd, Wd, idd, lpd, lse, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW)
             loss_host.copy_(loss, non_blocking=True)
 
         e2e_step()
@@ -367,7 +377,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generators; no dataset)",
-        "config": config_of(w),
+        "config": config_of(w, args.api),
         "tflops": tflops, "tflops_frac_of_peak": tflops / peak_sus,
         "peak_gib": peak_bytes / 2**30,
         "gpu_launches": launches,

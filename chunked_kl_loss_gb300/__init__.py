@@ -21,7 +21,7 @@ import ctypes
 import os
 
 __all__ = ["LIB_PATH", "FcklError", "load", "workspace_bytes", "Workspace", "forward", "backward",
-           "forward_backward", "check", "launch_count", "profile_enable", "profile_read",
+           "forward_backward", "fused_chunked_kl", "check", "launch_count", "profile_enable", "profile_read",
            "kernel_names", "OK", "ERR_ARG", "ERR_INDEX", "ERR_CUDA", "ERR_TIMEOUT",
            "ERR_WORKSPACE", "ERR_UNSUPPORTED"]
 
@@ -56,9 +56,14 @@ def load():
     lib.fckl_workspace_bytes.restype = sz
     lib.fckl_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
     lib.fckl_forward.restype = i32
-    lib.fckl_forward.argtypes = [vp, vp, i32, vp, vp, i64, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+    lib.fckl_forward.argtypes = [vp, vp, i32, vp, vp, vp, i64, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
     lib.fckl_backward.restype = i32
-    lib.fckl_backward.argtypes = [vp, vp, i32, vp, vp, vp, i64, i32, i32, i32, i32, f32, vp, vp, vp, sz, vp]
+    lib.fckl_backward.argtypes = [vp, vp, i32, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32, vp, vp, vp, sz, vp]
+    lib.fckl_forward_backward.restype = i32
+    lib.fckl_forward_backward.argtypes = [vp, vp, i32, vp, vp, vp, i64, i32, i32, i32, i32, f32, vp, vp, vp, vp,
+                                          vp, vp, sz, vp]
+    lib.fckl_selftest_wait_timeout.restype = i32
+    lib.fckl_selftest_wait_timeout.argtypes = [vp, sz, vp]
     lib.fckl_check.restype = i32
     lib.fckl_check.argtypes = [vp, vp]
     lib.fckl_status_string.restype = c.c_char_p
@@ -121,6 +126,17 @@ class Workspace:
 _last_ws = None
 
 
+def _weight(weight, N):
+    if weight is None:
+        return None
+    import torch
+    if tuple(weight.shape) != (N,) or not weight.is_cuda or not weight.is_contiguous():
+        raise ValueError("weight must be a contiguous CUDA tensor of shape [N]")
+    if weight.dtype != torch.float32:
+        raise TypeError("weight must be float32")
+    return weight
+
+
 def _shape(H, W, idx, logp):
     N, d = H.shape
     V = W.shape[0]
@@ -146,47 +162,101 @@ def _ws_for(ws, N, d, V, K, chunk, dt, device):
     return ws
 
 
-def forward(H, W, idx, logp, chunk, ws=None, stream=None, row_loss=False):
+def forward(H, W, idx, logp, chunk, ws=None, stream=None, row_loss=False, weight=None):
     """Returns (loss [1] fp32, lse [N] fp32) or, with ``row_loss=True``, also the
-    per-position losses [N]."""
+    per-position losses [N]. ``weight`` [N] fp32 scales each position's loss (0 = padding)."""
     import torch
     N, d, V, K = _shape(H, W, idx, logp)
+    weight = _weight(weight, N)
     dt = _dtype_code(H)
     ws = _ws_for(ws, N, d, V, K, chunk, dt, H.device)
     loss = torch.empty(1, dtype=torch.float32, device=H.device)
     lse = torch.empty(N, dtype=torch.float32, device=H.device)
     rl = torch.empty(N, dtype=torch.float32, device=H.device) if row_loss else None
-    st = load().fckl_forward(_ptr(H), _ptr(W), dt, _ptr(idx), _ptr(logp), N, d, V, K, chunk,
+    st = load().fckl_forward(_ptr(H), _ptr(W), dt, _ptr(idx), _ptr(logp), _ptr(weight), N, d, V, K, chunk,
                              _ptr(loss), _ptr(lse), _ptr(rl), ws.ptr, ws.nbytes, _stream_ptr(stream))
     if st != OK:
         raise FcklError(st, "fckl_forward")
     return (loss, lse, rl) if row_loss else (loss, lse)
 
 
-def backward(H, W, idx, logp, lse, chunk, grad_scale=1.0, ws=None, stream=None, dH=None, dW=None):
+def backward(H, W, idx, logp, lse, chunk, grad_scale=1.0, ws=None, stream=None, dH=None, dW=None,
+             weight=None):
     """Returns (dH [N,d] in H's dtype, dW [V,d] fp32)."""
     import torch
     N, d, V, K = _shape(H, W, idx, logp)
+    weight = _weight(weight, N)
     dt = _dtype_code(H)
     ws = _ws_for(ws, N, d, V, K, chunk, dt, H.device)
     if dH is None:
         dH = torch.empty_like(H)
     if dW is None:
         dW = torch.empty(V, d, dtype=torch.float32, device=H.device)
-    st = load().fckl_backward(_ptr(H), _ptr(W), dt, _ptr(idx), _ptr(logp), _ptr(lse), N, d, V, K, chunk,
-                              float(grad_scale), _ptr(dH), _ptr(dW), ws.ptr, ws.nbytes, _stream_ptr(stream))
+    st = load().fckl_backward(_ptr(H), _ptr(W), dt, _ptr(idx), _ptr(logp), _ptr(weight), _ptr(lse), N, d, V, K,
+                              chunk, float(grad_scale), _ptr(dH), _ptr(dW), ws.ptr, ws.nbytes, _stream_ptr(stream))
     if st != OK:
         raise FcklError(st, "fckl_backward")
     return dH, dW
 
 
-def forward_backward(H, W, idx, logp, chunk, grad_scale=1.0, ws=None, stream=None):
-    """(loss, lse, dH, dW) from one forward and one backward call sharing a workspace."""
+def forward_backward(H, W, idx, logp, chunk, grad_scale=1.0, ws=None, stream=None, weight=None,
+                     row_loss=False, dH=None, dW=None):
+    """(loss, lse, dH, dW) — or (loss, lse, row_loss, dH, dW) with ``row_loss=True`` — from
+    one fckl_forward_backward call (each chunk's backward right after its forward)."""
+    import torch
     N, d, V, K = _shape(H, W, idx, logp)
-    ws = _ws_for(ws, N, d, V, K, chunk, _dtype_code(H), H.device)
-    loss, lse = forward(H, W, idx, logp, chunk, ws=ws, stream=stream)
-    dH, dW = backward(H, W, idx, logp, lse, chunk, grad_scale=grad_scale, ws=ws, stream=stream)
-    return loss, lse, dH, dW
+    weight = _weight(weight, N)
+    dt = _dtype_code(H)
+    ws = _ws_for(ws, N, d, V, K, chunk, dt, H.device)
+    loss = torch.empty(1, dtype=torch.float32, device=H.device)
+    lse = torch.empty(N, dtype=torch.float32, device=H.device)
+    rl = torch.empty(N, dtype=torch.float32, device=H.device) if row_loss else None
+    if dH is None:
+        dH = torch.empty_like(H)
+    if dW is None:
+        dW = torch.empty(V, d, dtype=torch.float32, device=H.device)
+    st = load().fckl_forward_backward(_ptr(H), _ptr(W), dt, _ptr(idx), _ptr(logp), _ptr(weight), N, d, V, K,
+                                      chunk, float(grad_scale), _ptr(loss), _ptr(lse), _ptr(rl), _ptr(dH),
+                                      _ptr(dW), ws.ptr, ws.nbytes, _stream_ptr(stream))
+    if st != OK:
+        raise FcklError(st, "fckl_forward_backward")
+    return (loss, lse, rl, dH, dW) if row_loss else (loss, lse, dH, dW)
+
+
+def _autograd_function():
+    import torch
+
+    class FusedChunkedKL(torch.autograd.Function):
+        """Autograd wrapper: the forward keeps lse only; the backward recomputes each chunk's
+        logits (fckl_backward) with the upstream gradient as grad_scale. Reading the upstream
+        gradient synchronises with the device once per backward."""
+
+        @staticmethod
+        def forward(ctx, H, W, idx, logp, chunk, weight):
+            loss, lse = forward(H, W, idx, logp, chunk, weight=weight)
+            ctx.save_for_backward(H, W, idx, logp, lse, weight)
+            ctx.chunk = chunk
+            return loss[0]
+
+        @staticmethod
+        def backward(ctx, g):
+            H, W, idx, logp, lse, weight = ctx.saved_tensors
+            dH, dW = backward(H, W, idx, logp, lse, ctx.chunk, grad_scale=float(g), weight=weight)
+            return dH, dW, None, None, None, None
+
+    return FusedChunkedKL
+
+
+_FusedChunkedKL = None
+
+
+def fused_chunked_kl(H, W, idx, logp, chunk, weight=None):
+    """The loss as a differentiable scalar: gradients reach H and W through autograd (W's
+    fp32 gradient is cast to W's dtype by autograd)."""
+    global _FusedChunkedKL
+    if _FusedChunkedKL is None:
+        _FusedChunkedKL = _autograd_function()
+    return _FusedChunkedKL.apply(H, W, idx, logp, chunk, weight)
 
 
 def check(ws=None, stream=None, raise_on_error=True) -> int:

@@ -10,6 +10,8 @@
 //              -> dH = G W (tcgen05, split over V, fp32 partials) -> dH reduce
 //              -> dW (+)= G^T H_chunk (tcgen05, TMA store on the first chunk, TMA
 //                 reduce-add afterwards)
+// fckl_forward_backward runs both per chunk (lse of a position depends on its own row only),
+// ordering the chunk's cache slots once.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -37,11 +39,13 @@ enum Kind {
   KIND_BWD_DH_REDUCE,
   KIND_BWD_DW,
   KIND_CVT,
+  KIND_SELFTEST,
   KIND_COUNT
 };
 const char* const kKindNames[KIND_COUNT] = {"preprocess",     "fwd_logits_lse", "fwd_combine",
                                             "loss_reduce",    "bwd_logit_grad", "bwd_dH_gemm",
-                                            "bwd_dH_reduce",  "bwd_dW_gemm",    "cvt_bf16"};
+                                            "bwd_dH_reduce",  "bwd_dW_gemm",    "cvt_bf16",
+                                            "wait_timeout_selftest"};
 
 // ------------------------------------------------------------------ process state
 std::mutex g_mu;
@@ -338,6 +342,238 @@ int common_checks(const void* H, const void* W, int dt, const int32_t* idx, cons
   return device_info(di);
 }
 
+// Everything one call needs to run the per-chunk steps.
+struct Run {
+  Plan pl;
+  DevInfo* di = nullptr;
+  cudaStream_t s = nullptr;
+  uint8_t* w = nullptr;  // workspace
+  unsigned* status = nullptr;
+  const void* H = nullptr;
+  const void* Wb = nullptr;  // W as bf16 (the caller's W, or its bf16 copy)
+  int dtype = FCKL_BF16;
+  const int32_t* idx = nullptr;
+  const float* logp = nullptr;
+  const float* weight = nullptr;  // [N] or null
+  float* lse = nullptr;           // [N]
+  float* rl = nullptr;            // [N] per-position loss
+  float grad_scale = 1.f;
+  void* dH = nullptr;
+  float* dW = nullptr;
+  int splits = 1;  // K-splits of the dH product
+  CUtensorMap tmW_k, tmW_mn, tmDW, tmDWp;
+};
+
+// Clears the status word, rounds fp32 W to bf16 when needed and encodes the maps over W
+// (and dW) shared by every chunk.
+int run_begin(Run& r, bool backward) {
+  const Plan& pl = r.pl;
+  cudaError_t e = cudaMemsetAsync(r.status, 0, sizeof(unsigned), r.s);
+  if (e != cudaSuccess) {
+    set_error("cudaMemsetAsync", e);
+    return FCKL_ERR_CUDA;
+  }
+  int st;
+  if (r.dtype == FCKL_F32) {
+    if ((st = launch_cvt(static_cast<const float*>(r.Wb), r.w + pl.off_Wb, int64_t(pl.V) * pl.d, r.di, r.s)))
+      return st;
+    r.Wb = r.w + pl.off_Wb;
+  }
+  const int d = pl.d, V = pl.V;
+  if ((st = make_map(&r.tmW_k, r.Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK, VOCAB_TILE / CG)))
+    return st;
+  if (!backward) return FCKL_OK;
+  if ((st = make_map(&r.tmW_mn, r.Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, 64, BK))) return st;
+  if ((st = make_map(&r.tmDW, r.dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, V, uint64_t(d) * 4, 32, 32))) return st;
+  if ((st = make_map(&r.tmDWp, r.dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, V, uint64_t(d) * 4, 256, BM,
+                     CU_TENSOR_MAP_SWIZZLE_NONE)))
+    return st;
+  // K-splits of dH = G W (K = V): the count that best fills the SM pairs.
+  const int kb_v = static_cast<int>(cdiv(V, BK));
+  const int tiles = static_cast<int>(cdiv(pl.chunk, TILE_M) * cdiv(d, pl.bn_d));
+  double best = -1.0;
+  for (int sp = 1; sp <= MAX_SPLITS && sp <= kb_v; ++sp) {
+    const int kbps = static_cast<int>(cdiv(kb_v, sp));
+    if (cdiv(kb_v, kbps) != sp) continue;
+    const int64_t units = int64_t(tiles) * sp;
+    const int64_t slots = r.di->sms / CG;
+    const double eff = double(units) / double(cdiv(units, slots) * slots);
+    if (eff > best + 0.02) {
+      best = eff;
+      r.splits = sp;
+    }
+  }
+  return FCKL_OK;
+}
+
+// Orders the chunk's cache slots (and rounds an fp32 chunk of H); returns the chunk's H rows.
+int chunk_prepare(Run& r, int64_t r0, int rows, const void** Hc) {
+  const Plan& pl = r.pl;
+  int st = launch_preprocess(pl, r.idx + r0 * pl.K, r.logp + r0 * pl.K, rows, r.w, r.status, r.di, r.s);
+  if (st) return st;
+  const size_t esz = r.dtype == FCKL_F32 ? 4 : 2;
+  *Hc = static_cast<const uint8_t*>(r.H) + static_cast<size_t>(r0) * pl.d * esz;
+  if (r.dtype == FCKL_F32) {
+    if ((st = launch_cvt(static_cast<const float*>(*Hc), r.w + pl.off_Hb, int64_t(rows) * pl.d, r.di, r.s)))
+      return st;
+    *Hc = r.w + pl.off_Hb;
+  }
+  return FCKL_OK;
+}
+
+// Forward of one chunk: logits tiles -> per-tile (max, sum-exp, gathered sum) -> lse and loss.
+int chunk_forward(Run& r, int64_t r0, int rows, const void* Hc) {
+  const Plan& pl = r.pl;
+  const int d = pl.d;
+  uint8_t* w = r.w;
+  int st;
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  if ((st = make_map(&p.tmA, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM))) return st;
+  p.tmB = r.tmW_k;
+  p.sch = {static_cast<int>(cdiv(rows, TILE_M)), pl.tiles_v, static_cast<int>(cdiv(d, BK)), 1,
+           static_cast<int>(cdiv(d, BK)), 1};
+  p.num_units = p.sch.m_blocks * p.sch.n_blocks;
+  p.status = r.status;
+  p.rows_valid = rows;
+  p.V = pl.V;
+  p.K = pl.K;
+  p.sidx = reinterpret_cast<const int*>(w + pl.off_sidx);
+  p.sp = reinterpret_cast<const float*>(w + pl.off_sp);
+  p.S = reinterpret_cast<const float*>(w + pl.off_S);
+  p.pm = reinterpret_cast<float*>(w + pl.off_pm);
+  p.pl = reinterpret_cast<float*>(w + pl.off_pl);
+  p.pc = reinterpret_cast<float*>(w + pl.off_pc);
+  p.ld_part = pl.rows_alloc;
+  if ((st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_STATS>(KIND_FWD_LOGITS, r.di, p, r.s, "fwd_logits_lse")))
+    return st;
+  const int cblocks = static_cast<int>(cdiv(rows, 32));
+  const float* wc = r.weight ? r.weight + r0 : nullptr;
+  cudaStream_t s = r.s;
+  float* lse = r.lse + r0;
+  float* rl = r.rl + r0;
+  return launch(KIND_FWD_COMBINE, s, "fwd_combine", [&] {
+    combine_kernel<<<cblocks, 256, 0, s>>>(p.pm, p.pl, p.pc, pl.rows_alloc, pl.tiles_v, rows, p.S,
+                                           reinterpret_cast<const float*>(w + pl.off_T), wc, lse, rl);
+  });
+}
+
+// Backward of one chunk: recompute the logits into G, then dH_chunk = G W and dW (+)= G^T H_chunk.
+int chunk_backward(Run& r, int64_t r0, int rows, const void* Hc) {
+  const Plan& pl = r.pl;
+  const int d = pl.d, V = pl.V;
+  uint8_t* w = r.w;
+  cudaStream_t s = r.s;
+  void* G = w + pl.off_G;
+  float* dhp = reinterpret_cast<float*>(w + pl.off_dhp);
+  const int mbr = static_cast<int>(cdiv(rows, TILE_M));
+  const int kb_v = static_cast<int>(cdiv(V, BK));
+  int st;
+
+  // --- G = scale * w_n * (S softmax(z) - p_sparse), z recomputed
+  TcParams pg;
+  memset(&pg, 0, sizeof(pg));
+  if ((st = make_map(&pg.tmA, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM))) return st;
+  pg.tmB = r.tmW_k;
+  if ((st = make_map(&pg.tmC, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, uint64_t(pl.ldG) * 2, 64, 32)))
+    return st;
+  pg.sch = {mbr, pl.tiles_v, static_cast<int>(cdiv(d, BK)), 1, static_cast<int>(cdiv(d, BK)), 1};
+  pg.num_units = mbr * pl.tiles_v;
+  pg.status = r.status;
+  pg.rows_valid = rows;
+  pg.V = V;
+  pg.K = pl.K;
+  pg.sidx = reinterpret_cast<const int*>(w + pl.off_sidx);
+  pg.sp = reinterpret_cast<const float*>(w + pl.off_sp);
+  pg.S = reinterpret_cast<const float*>(w + pl.off_S);
+  pg.lse = r.lse + r0;
+  pg.wrow = r.weight ? r.weight + r0 : nullptr;
+  pg.gscale = r.grad_scale;
+  pg.c_xlim = V;
+  pg.c_ylim = rows;
+  if ((st = launch_tc<VOCAB_TILE, false, false, EPI_LOGIT_GRAD>(KIND_BWD_GRAD, r.di, pg, s, "bwd_logit_grad")))
+    return st;
+
+  // --- dH_chunk = G W, split over the vocabulary into fp32 partials, then summed
+  const int nbd = static_cast<int>(cdiv(d, pl.bn_d));
+  const int splits = r.splits;
+  TcParams ph;
+  memset(&ph, 0, sizeof(ph));
+  if ((st = make_map(&ph.tmA, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, uint64_t(pl.ldG) * 2, BK, BM))) return st;
+  ph.tmB = r.tmW_mn;
+  if ((st = make_map(&ph.tmC, dhp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, uint64_t(splits) * pl.rows_alloc,
+                     uint64_t(d) * 4, 32, 32)))
+    return st;
+  const int kbps = static_cast<int>(cdiv(kb_v, splits));
+  ph.sch = {mbr, nbd, kb_v, splits, kbps, 0};
+  ph.num_units = mbr * nbd * splits;
+  ph.status = r.status;
+  ph.c_split_rows = pl.rows_alloc;
+  ph.c_reduce = 0;
+  ph.c_xlim = d;
+  ph.c_ylim = splits * pl.rows_alloc;
+  if ((st = launch_tc<256, false, true, EPI_STORE_F32>(KIND_BWD_DH, r.di, ph, s, "bwd_dH_gemm"))) return st;
+  {
+    const int64_t n4 = int64_t(rows) * d / 4;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(n4, 256), int64_t(r.di->sms) * 8)));
+    const int64_t stride = int64_t(pl.rows_alloc) * d;
+    if (r.dtype == FCKL_F32) {
+      float* out = static_cast<float*>(r.dH) + static_cast<size_t>(r0) * d;
+      st = launch(KIND_BWD_DH_REDUCE, s, "bwd_dH_reduce",
+                  [&] { dh_reduce_kernel<float><<<grid, 256, 0, s>>>(dhp, splits, stride, rows, d, out); });
+    } else {
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(r.dH) + static_cast<size_t>(r0) * d;
+      st = launch(KIND_BWD_DH_REDUCE, s, "bwd_dH_reduce", [&] {
+        dh_reduce_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(dhp, splits, stride, rows, d, out);
+      });
+    }
+    if (st) return st;
+  }
+
+  // --- dW (+)= G^T H_chunk: the first chunk stores, later chunks reduce-add
+  TcParams pw;
+  memset(&pw, 0, sizeof(pw));
+  if ((st = make_map(&pw.tmA, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, uint64_t(pl.ldG) * 2, 64, BK))) return st;
+  if ((st = make_map(&pw.tmB, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, 64, BK))) return st;
+  pw.tmC = r.tmDW;
+  pw.tmP = r.tmDWp;
+  const int kb_r = static_cast<int>(cdiv(rows, BK));
+  pw.sch = {static_cast<int>(cdiv(V, TILE_M)), nbd, kb_r, 1, kb_r, 0};
+  pw.num_units = pw.sch.m_blocks * nbd;
+  pw.status = r.status;
+  pw.c_split_rows = 0;
+  pw.c_reduce = r0 > 0 ? 1 : 0;
+  pw.c_prefetch = pw.c_reduce;
+  pw.c_xlim = d;
+  pw.c_ylim = V;
+  return launch_tc<256, true, true, EPI_STORE_F32>(KIND_BWD_DW, r.di, pw, s, "bwd_dW_gemm");
+}
+
+int run_loss(Run& r, float* loss) {
+  const float* rl = r.rl;
+  const int64_t N = r.pl.N;
+  cudaStream_t s = r.s;
+  return launch(KIND_LOSS_REDUCE, s, "loss_reduce", [&] { loss_reduce_kernel<<<1, 1024, 0, s>>>(rl, N, loss); });
+}
+
+int run_setup(Run& r, const void* H, const void* W, int dtype, const int32_t* idx, const float* logp,
+              const float* weight, int64_t N, int d, int V, int K, int chunk, void* ws, size_t ws_bytes,
+              void* stream) {
+  int st = common_checks(H, W, dtype, idx, logp, N, d, V, K, chunk, ws, ws_bytes, &r.pl, &r.di);
+  if (st) return st;
+  if (!aligned(weight, 4)) return FCKL_ERR_ARG;
+  r.s = static_cast<cudaStream_t>(stream);
+  r.w = static_cast<uint8_t*>(ws);
+  r.status = reinterpret_cast<unsigned*>(r.w + r.pl.off_status);
+  r.H = H;
+  r.Wb = W;
+  r.dtype = dtype;
+  r.idx = idx;
+  r.logp = logp;
+  r.weight = weight;
+  return FCKL_OK;
+}
+
 }  // namespace
 }  // namespace fckl
 
@@ -350,209 +586,86 @@ size_t fckl_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype
   return make_plan(N, d, V, K, chunk, dtype).total;
 }
 
-int fckl_forward(const void* H, const void* W, int dtype, const int32_t* idx, const float* logp, int64_t N, int d,
-                 int V, int K, int chunk, float* loss, float* lse, float* row_loss, void* ws, size_t ws_bytes,
-                 void* stream) {
-  Plan pl;
-  DevInfo* di = nullptr;
-  int st = common_checks(H, W, dtype, idx, logp, N, d, V, K, chunk, ws, ws_bytes, &pl, &di);
+int fckl_forward(const void* H, const void* W, int dtype, const int32_t* idx, const float* logp,
+                 const float* weight, int64_t N, int d, int V, int K, int chunk, float* loss, float* lse,
+                 float* row_loss, void* ws, size_t ws_bytes, void* stream) {
+  Run r;
+  int st = run_setup(r, H, W, dtype, idx, logp, weight, N, d, V, K, chunk, ws, ws_bytes, stream);
   if (st) return st;
   if (!loss || !lse || !aligned(loss, 4) || !aligned(lse, 4) || !aligned(row_loss, 4)) return FCKL_ERR_ARG;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  float* rl = row_loss ? row_loss : reinterpret_cast<float*>(w + pl.off_rowloss);
-  unsigned* status = reinterpret_cast<unsigned*>(w + pl.off_status);
-  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(unsigned), s);
-  if (e != cudaSuccess) {
-    set_error("cudaMemsetAsync", e);
-    return FCKL_ERR_CUDA;
+  r.lse = lse;
+  r.rl = row_loss ? row_loss : reinterpret_cast<float*>(r.w + r.pl.off_rowloss);
+  if ((st = run_begin(r, false))) return st;
+  for (int64_t r0 = 0; r0 < N; r0 += r.pl.chunk) {
+    const int rows = static_cast<int>(std::min<int64_t>(r.pl.chunk, N - r0));
+    const void* Hc = nullptr;
+    if ((st = chunk_prepare(r, r0, rows, &Hc))) return st;
+    if ((st = chunk_forward(r, r0, rows, Hc))) return st;
   }
-  const void* Wb = W;
-  if (dtype == FCKL_F32) {
-    if ((st = launch_cvt(static_cast<const float*>(W), w + pl.off_Wb, int64_t(V) * d, di, s))) return st;
-    Wb = w + pl.off_Wb;
-  }
-  CUtensorMap tmW;
-  if ((st = make_map(&tmW, Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK, VOCAB_TILE / CG))) return st;
-  const size_t esz = dtype == FCKL_F32 ? 4 : 2;
-  for (int64_t r0 = 0; r0 < N; r0 += pl.chunk) {
-    const int rows = static_cast<int>(std::min<int64_t>(pl.chunk, N - r0));
-    if ((st = launch_preprocess(pl, idx + r0 * K, logp + r0 * K, rows, w, status, di, s))) return st;
-    const void* Hc = static_cast<const uint8_t*>(H) + static_cast<size_t>(r0) * d * esz;
-    if (dtype == FCKL_F32) {
-      if ((st = launch_cvt(static_cast<const float*>(Hc), w + pl.off_Hb, int64_t(rows) * d, di, s))) return st;
-      Hc = w + pl.off_Hb;
-    }
-    TcParams p;
-    memset(&p, 0, sizeof(p));
-    if ((st = make_map(&p.tmA, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM))) return st;
-    p.tmB = tmW;
-    p.sch = {static_cast<int>(cdiv(rows, TILE_M)), pl.tiles_v, static_cast<int>(cdiv(d, BK)), 1,
-             static_cast<int>(cdiv(d, BK)), 1};
-    p.num_units = p.sch.m_blocks * p.sch.n_blocks;
-    p.status = status;
-    p.rows_valid = rows;
-    p.V = V;
-    p.K = K;
-    p.sidx = reinterpret_cast<const int*>(w + pl.off_sidx);
-    p.sp = reinterpret_cast<const float*>(w + pl.off_sp);
-    p.S = reinterpret_cast<const float*>(w + pl.off_S);
-    p.pm = reinterpret_cast<float*>(w + pl.off_pm);
-    p.pl = reinterpret_cast<float*>(w + pl.off_pl);
-    p.pc = reinterpret_cast<float*>(w + pl.off_pc);
-    p.ld_part = pl.rows_alloc;
-    if ((st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_STATS>(KIND_FWD_LOGITS, di, p, s, "fwd_logits_lse")))
-      return st;
-    const int cblocks = static_cast<int>(cdiv(rows, 32));
-    if ((st = launch(KIND_FWD_COMBINE, s, "fwd_combine", [&] {
-           combine_kernel<<<cblocks, 256, 0, s>>>(p.pm, p.pl, p.pc, pl.rows_alloc, pl.tiles_v, rows, p.S,
-                                                  reinterpret_cast<const float*>(w + pl.off_T), lse + r0, rl + r0);
-         })))
-      return st;
-  }
-  return launch(KIND_LOSS_REDUCE, s, "loss_reduce", [&] {
-    loss_reduce_kernel<<<1, 1024, 0, s>>>(rl, N, loss);
-  });
+  return run_loss(r, loss);
 }
 
-int fckl_backward(const void* H, const void* W, int dtype, const int32_t* idx, const float* logp, const float* lse,
-                  int64_t N, int d, int V, int K, int chunk, float grad_scale, void* dH, float* dW, void* ws,
-                  size_t ws_bytes, void* stream) {
-  Plan pl;
-  DevInfo* di = nullptr;
-  int st = common_checks(H, W, dtype, idx, logp, N, d, V, K, chunk, ws, ws_bytes, &pl, &di);
+int fckl_backward(const void* H, const void* W, int dtype, const int32_t* idx, const float* logp,
+                  const float* weight, const float* lse, int64_t N, int d, int V, int K, int chunk,
+                  float grad_scale, void* dH, float* dW, void* ws, size_t ws_bytes, void* stream) {
+  Run r;
+  int st = run_setup(r, H, W, dtype, idx, logp, weight, N, d, V, K, chunk, ws, ws_bytes, stream);
   if (st) return st;
   if (!lse || !dH || !dW || !aligned(lse, 4) || !aligned(dH, 16) || !aligned(dW, 16)) return FCKL_ERR_ARG;
+  r.lse = const_cast<float*>(lse);
+  r.grad_scale = grad_scale;
+  r.dH = dH;
+  r.dW = dW;
+  if ((st = run_begin(r, true))) return st;
+  for (int64_t r0 = 0; r0 < N; r0 += r.pl.chunk) {
+    const int rows = static_cast<int>(std::min<int64_t>(r.pl.chunk, N - r0));
+    const void* Hc = nullptr;
+    if ((st = chunk_prepare(r, r0, rows, &Hc))) return st;
+    if ((st = chunk_backward(r, r0, rows, Hc))) return st;
+  }
+  return FCKL_OK;
+}
+
+int fckl_forward_backward(const void* H, const void* W, int dtype, const int32_t* idx, const float* logp,
+                          const float* weight, int64_t N, int d, int V, int K, int chunk, float grad_scale,
+                          float* loss, float* lse, float* row_loss, void* dH, float* dW, void* ws, size_t ws_bytes,
+                          void* stream) {
+  Run r;
+  int st = run_setup(r, H, W, dtype, idx, logp, weight, N, d, V, K, chunk, ws, ws_bytes, stream);
+  if (st) return st;
+  if (!loss || !lse || !dH || !dW || !aligned(loss, 4) || !aligned(lse, 4) || !aligned(row_loss, 4) ||
+      !aligned(dH, 16) || !aligned(dW, 16))
+    return FCKL_ERR_ARG;
+  r.lse = lse;
+  r.rl = row_loss ? row_loss : reinterpret_cast<float*>(r.w + r.pl.off_rowloss);
+  r.grad_scale = grad_scale;
+  r.dH = dH;
+  r.dW = dW;
+  if ((st = run_begin(r, true))) return st;
+  for (int64_t r0 = 0; r0 < N; r0 += r.pl.chunk) {
+    const int rows = static_cast<int>(std::min<int64_t>(r.pl.chunk, N - r0));
+    const void* Hc = nullptr;
+    if ((st = chunk_prepare(r, r0, rows, &Hc))) return st;
+    if ((st = chunk_forward(r, r0, rows, Hc))) return st;
+    if ((st = chunk_backward(r, r0, rows, Hc))) return st;
+  }
+  return run_loss(r, loss);
+}
+
+int fckl_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || !aligned(ws, 256) || ws_bytes < 256) return FCKL_ERR_ARG;
+  DevInfo* di = nullptr;
+  int st = device_info(&di);
+  if (st) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  unsigned* status = reinterpret_cast<unsigned*>(w + pl.off_status);
+  unsigned* status = static_cast<unsigned*>(ws);
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(unsigned), s);
   if (e != cudaSuccess) {
     set_error("cudaMemsetAsync", e);
     return FCKL_ERR_CUDA;
   }
-  const void* Wb = W;
-  if (dtype == FCKL_F32) {
-    if ((st = launch_cvt(static_cast<const float*>(W), w + pl.off_Wb, int64_t(V) * d, di, s))) return st;
-    Wb = w + pl.off_Wb;
-  }
-  const int bn = pl.bn_d;
-  CUtensorMap tmW_k, tmW_mn, tmDW, tmDWp;
-  if ((st = make_map(&tmW_k, Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK, VOCAB_TILE / CG))) return st;
-  if ((st = make_map(&tmW_mn, Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, 64, BK))) return st;
-  if ((st = make_map(&tmDW, dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, V, uint64_t(d) * 4, 32, 32))) return st;
-  if ((st = make_map(&tmDWp, dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, V, uint64_t(d) * 4, 256, BM,
-                     CU_TENSOR_MAP_SWIZZLE_NONE)))
-    return st;
-  void* G = w + pl.off_G;
-  float* dhp = reinterpret_cast<float*>(w + pl.off_dhp);
-  const size_t esz = dtype == FCKL_F32 ? 4 : 2;
-  const int kb_v = static_cast<int>(cdiv(V, BK));
-
-  for (int64_t r0 = 0; r0 < N; r0 += pl.chunk) {
-    const int rows = static_cast<int>(std::min<int64_t>(pl.chunk, N - r0));
-    const int mbr = static_cast<int>(cdiv(rows, TILE_M));
-    if ((st = launch_preprocess(pl, idx + r0 * K, logp + r0 * K, rows, w, status, di, s))) return st;
-    const void* Hc = static_cast<const uint8_t*>(H) + static_cast<size_t>(r0) * d * esz;
-    if (dtype == FCKL_F32) {
-      if ((st = launch_cvt(static_cast<const float*>(Hc), w + pl.off_Hb, int64_t(rows) * d, di, s))) return st;
-      Hc = w + pl.off_Hb;
-    }
-    // --- G = scale * (S softmax(z) - p_sparse) for the chunk, z recomputed
-    TcParams pg;
-    memset(&pg, 0, sizeof(pg));
-    if ((st = make_map(&pg.tmA, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM))) return st;
-    pg.tmB = tmW_k;
-    if ((st = make_map(&pg.tmC, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, uint64_t(pl.ldG) * 2, 64, 32)))
-      return st;
-    pg.sch = {mbr, pl.tiles_v, static_cast<int>(cdiv(d, BK)), 1, static_cast<int>(cdiv(d, BK)), 1};
-    pg.num_units = mbr * pl.tiles_v;
-    pg.status = status;
-    pg.rows_valid = rows;
-    pg.V = V;
-    pg.K = K;
-    pg.sidx = reinterpret_cast<const int*>(w + pl.off_sidx);
-    pg.sp = reinterpret_cast<const float*>(w + pl.off_sp);
-    pg.S = reinterpret_cast<const float*>(w + pl.off_S);
-    pg.lse = lse + r0;
-    pg.gscale = grad_scale;
-    pg.c_xlim = V;
-    pg.c_ylim = rows;
-    if ((st = launch_tc<VOCAB_TILE, false, false, EPI_LOGIT_GRAD>(KIND_BWD_GRAD, di, pg, s, "bwd_logit_grad")))
-      return st;
-
-    // --- dH_chunk = G W, split over the vocabulary into fp32 partials
-    const int nbd = static_cast<int>(cdiv(d, bn));
-    const int tiles = mbr * nbd;
-    int splits = 1;
-    {
-      double best = -1.0;
-      for (int sp = 1; sp <= MAX_SPLITS && sp <= kb_v; ++sp) {
-        const int kbps = static_cast<int>(cdiv(kb_v, sp));
-        if (cdiv(kb_v, kbps) != sp) continue;
-        const int64_t units = int64_t(tiles) * sp;
-        const int64_t slots = di->sms / CG;
-        const double eff = double(units) / double(cdiv(units, slots) * slots);
-        if (eff > best + 0.02) {
-          best = eff;
-          splits = sp;
-        }
-      }
-    }
-    TcParams ph;
-    memset(&ph, 0, sizeof(ph));
-    if ((st = make_map(&ph.tmA, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, uint64_t(pl.ldG) * 2, BK, BM)))
-      return st;
-    ph.tmB = tmW_mn;
-    if ((st = make_map(&ph.tmC, dhp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, uint64_t(splits) * pl.rows_alloc,
-                       uint64_t(d) * 4, 32, 32)))
-      return st;
-    const int kbps = static_cast<int>(cdiv(kb_v, splits));
-    ph.sch = {mbr, nbd, kb_v, splits, kbps, 0};
-    ph.num_units = tiles * splits;
-    ph.status = status;
-    ph.c_split_rows = pl.rows_alloc;
-    ph.c_reduce = 0;
-    ph.c_xlim = d;
-    ph.c_ylim = splits * pl.rows_alloc;
-    if ((st = launch_tc<256, false, true, EPI_STORE_F32>(KIND_BWD_DH, di, ph, s, "bwd_dH_gemm"))) return st;
-    {
-      const int64_t n4 = int64_t(rows) * d / 4;
-      const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(n4, 256), int64_t(di->sms) * 8)));
-      const int64_t stride = int64_t(pl.rows_alloc) * d;
-      if (dtype == FCKL_F32) {
-        float* out = static_cast<float*>(dH) + static_cast<size_t>(r0) * d;
-        st = launch(KIND_BWD_DH_REDUCE, s, "bwd_dH_reduce",
-                    [&] { dh_reduce_kernel<float><<<grid, 256, 0, s>>>(dhp, splits, stride, rows, d, out); });
-      } else {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(dH) + static_cast<size_t>(r0) * d;
-        st = launch(KIND_BWD_DH_REDUCE, s, "bwd_dH_reduce", [&] {
-          dh_reduce_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(dhp, splits, stride, rows, d, out);
-        });
-      }
-      if (st) return st;
-    }
-
-    // --- dW (+)= G^T H_chunk
-    TcParams pw;
-    memset(&pw, 0, sizeof(pw));
-    if ((st = make_map(&pw.tmA, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, uint64_t(pl.ldG) * 2, 64, BK)))
-      return st;
-    if ((st = make_map(&pw.tmB, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, 64, BK))) return st;
-    pw.tmC = tmDW;
-    pw.tmP = tmDWp;
-    const int kb_r = static_cast<int>(cdiv(rows, BK));
-    pw.sch = {static_cast<int>(cdiv(V, TILE_M)), nbd, kb_r, 1, kb_r, 0};
-    pw.num_units = pw.sch.m_blocks * nbd;
-    pw.status = status;
-    pw.c_split_rows = 0;
-    pw.c_reduce = r0 > 0 ? 1 : 0;
-    pw.c_prefetch = pw.c_reduce;
-    pw.c_xlim = d;
-    pw.c_ylim = V;
-    if ((st = launch_tc<256, true, true, EPI_STORE_F32>(KIND_BWD_DW, di, pw, s, "bwd_dW_gemm"))) return st;
-  }
-  return FCKL_OK;
+  return launch(KIND_SELFTEST, s, "wait_timeout_selftest",
+                [&] { wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(status, 50000000ull); });
 }
 
 int fckl_check(void* ws, void* stream) {
@@ -744,8 +857,8 @@ extern "C" int fckl_forward_static(const void* H, const void* W, int dtype, cons
     const int cblocks = static_cast<int>(cdiv(rows, 32));
     if ((st = launch(KIND_FWD_COMBINE, s, "fwd_combine", [&] {
            combine_kernel<<<cblocks, 256, 0, s>>>(p.pm, p.pl, p.pc, pl.rows_alloc, pl.tiles_v, rows, p.S,
-                                                  reinterpret_cast<const float*>(w + pl.off_T), lse + r0,
-                                                  row_loss + r0);
+                                                  reinterpret_cast<const float*>(w + pl.off_T), nullptr,
+                                                  lse + r0, row_loss + r0);
          })))
       return st;
   }

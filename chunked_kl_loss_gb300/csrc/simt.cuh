@@ -66,12 +66,14 @@ __global__ void __launch_bounds__(32 * PRE_WARPS) preprocess_kernel(
 
 // Merge the (m, l, c) statistics of every vocabulary tile of a position:
 //   lse_n  = M + log sum_t l_t exp(m_t - M),   c_n = sum_t c_t
-//   loss_n = T_n - c_n + S_n lse_n             (= sum_k p_nk (logp_nk - z_{n,idx_nk} + lse_n))
-// 32 positions per block; 8 warps split the tiles and are merged in a fixed order.
+//   loss_n = w_n (T_n - c_n + S_n lse_n)       (= w_n sum_k p_nk (logp_nk - z_{n,idx_nk} + lse_n))
+// with w_n = 1 when no weights are given. 32 positions per block; 8 warps split the tiles
+// and are merged in a fixed order.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
                                                       const float* __restrict__ pc, int ld, int tiles, int rows,
                                                       const float* __restrict__ S, const float* __restrict__ T,
-                                                      float* __restrict__ lse_out, float* __restrict__ loss_out) {
+                                                      const float* __restrict__ weight, float* __restrict__ lse_out,
+                                                      float* __restrict__ loss_out) {
   __shared__ float sm[8][32], sl[8][32], sc[8][32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int row = blockIdx.x * 32 + lane;
@@ -102,7 +104,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     }
     const float lse = M + logf(Lr);
     lse_out[row] = lse;
-    loss_out[row] = T[row] - C + S[row] * lse;
+    const float wn = weight ? weight[row] : 1.f;
+    loss_out[row] = wn * (T[row] - C + S[row] * lse);
   }
 }
 

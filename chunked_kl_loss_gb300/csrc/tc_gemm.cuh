@@ -17,8 +17,8 @@
 //                   the gather of the logits at the teacher's cached ids; writes one
 //                   (m, l, c) triple per row and vocabulary tile ("Fused, chunked KL loss":
 //                   fold the chunk's logits into the running loss, then drop them)
-//   EPI_LOGIT_GRAD: G = scale * (S_n exp(z - lse_n) - p at the cached ids), rounded to
-//                   bf16 and stored with TMA (the backward pass recomputes the chunk)
+//   EPI_LOGIT_GRAD: G = scale * w_n * (S_n exp(z - lse_n) - p at the cached ids), rounded
+//                   to bf16 and stored with TMA (the backward pass recomputes the chunk)
 //   EPI_STORE_F32 : fp32 tile stored, or reduce-added, with TMA (dH partials, dW)
 // Every wait is bounded by WAIT_TIMEOUT_NS; on expiry the CTA records FCKL status bit
 // ST_TIMEOUT, lets its copies and MMAs in flight drain, frees TMEM and returns.
@@ -65,6 +65,7 @@ struct TcParams {
   const float* sp;   // [rows][K] matching teacher probabilities
   const float* S;    // [rows] kept teacher mass
   const float* lse;  // [rows] log-partition (backward)
+  const float* wrow;  // [rows] position weights, or null for all ones (backward)
   float gscale;
   float* pm;
   float* pl;
@@ -113,14 +114,14 @@ __device__ __forceinline__ void decode_unit(const Sched& s, int u, int& mb, int&
 // CTA is aborting (another role gave up) or when the deadline passed (then it also raises
 // the abort flag and the status bit).
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                           unsigned* status) {
+                                           unsigned* status, uint64_t timeout_ns = WAIT_TIMEOUT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > WAIT_TIMEOUT_NS) {
+      if (globaltimer_ns() - t0 > timeout_ns) {
         *abort_flag = 1;
         atomicOr(status, ST_TIMEOUT);
         return false;
@@ -177,6 +178,20 @@ __device__ __forceinline__ void sub32(float (&x)[32], int pos, float v) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Self-test of the bounded wait: one thread waits on a barrier that nothing arrives at; the
+// wait gives up after timeout_ns, records ST_TIMEOUT and the kernel returns normally.
+__global__ void wait_timeout_selftest_kernel(unsigned* status, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) wait_phase(&bar, 0, &abort_flag, status, timeout_ns);
 }
 
 // Bounded wait whose acquire also covers arrivals from the peer CTA of a pair.
@@ -440,7 +455,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             p.pc[o] = c;
           }
         } else {
-          const float a = valid ? p.gscale * __ldg(p.S + row) : 0.f;
+          const float gs = valid ? p.gscale * (p.wrow ? __ldg(p.wrow + row) : 1.f) : 0.f;
+          const float a = gs * (valid ? __ldg(p.S + row) : 0.f);
           const float nl = valid ? -__ldg(p.lse + row) * LOG2E : 0.f;
           if (!warp_wait_phase(&tfull[acc], use & 1u, abort_flag, p.status)) break;
           tc_fence_after();
@@ -460,7 +476,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 #pragma unroll
               for (int t = 0; t < 32; ++t) x[t] = a * ex2_approx(fmaf(x[t], LOG2E, nl));
               while (nxt < cb + 32) {
-                sub32(x, nxt - cb, p.gscale * __ldg(pr + k));
+                sub32(x, nxt - cb, gs * __ldg(pr + k));
                 ++k;
                 nxt = k < p.K ? __ldg(ids + k) : INT_MAX;
               }

@@ -26,6 +26,10 @@
  *  - idx is int32 [N, K]: teacher token ids, any order, each in [0, V). logp is fp32 [N, K]:
  *    the teacher's log-probabilities for those ids; -inf marks an empty slot. A repeated
  *    id within a row contributes once per slot.
+ *  - weight is fp32 [N] or NULL (all ones): position n contributes weight[n] * loss_n to the
+ *    loss and weight[n] * G_n to the gradients; 0 drops a padded position (sequence packing
+ *    is among the ablations of "Hugging Face：让知识蒸馏廉价到可大规模运行", section "得到的
+ *    student"). lse is not weighted.
  *  - `stream` is a cudaStream_t (may be NULL for the legacy default stream). Every call is
  *    asynchronous on it; inputs must stay alive and unmodified until the work completes.
  *  - Limits: N >= 1, 1 <= K <= min(V, 1024), d % 8 == 0 (16-byte rows for the tensor
@@ -70,7 +74,7 @@ size_t fckl_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype
  *   row_loss : device fp32 [N]  <- per-position KL, or NULL when not wanted
  * Overwrites the workspace and clears its status word first. */
 int fckl_forward(const void* H, const void* W, int dtype,
-                 const int32_t* idx, const float* logp,
+                 const int32_t* idx, const float* logp, const float* weight,
                  int64_t N, int d, int V, int K, int chunk,
                  float* loss, float* lse, float* row_loss,
                  void* ws, size_t ws_bytes, void* stream);
@@ -82,10 +86,20 @@ int fckl_forward(const void* H, const void* W, int dtype,
  *   dW         : device fp32 [V, d], overwritten
  * Overwrites the workspace and clears its status word first. */
 int fckl_backward(const void* H, const void* W, int dtype,
-                  const int32_t* idx, const float* logp, const float* lse,
+                  const int32_t* idx, const float* logp, const float* weight, const float* lse,
                   int64_t N, int d, int V, int K, int chunk,
                   float grad_scale, void* dH, float* dW,
                   void* ws, size_t ws_bytes, void* stream);
+
+/* Forward and backward in one call, chunk by chunk: each chunk's backward runs right after
+ * its forward (lse_n depends on position n alone), so the chunk's cache slots are ordered
+ * once and its hidden states are re-read while still in L2. Outputs as fckl_forward and
+ * fckl_backward (row_loss may be NULL); same workspace size. */
+int fckl_forward_backward(const void* H, const void* W, int dtype,
+                          const int32_t* idx, const float* logp, const float* weight,
+                          int64_t N, int d, int V, int K, int chunk, float grad_scale,
+                          float* loss, float* lse, float* row_loss, void* dH, float* dW,
+                          void* ws, size_t ws_bytes, void* stream);
 
 /* Largest device scratch (bytes) that fckl_forward_static can use. The library reserves this
  * much device memory on every GPU where it is loaded, and keeps it until the process exits. */
@@ -125,6 +139,13 @@ int fckl_forward_static(const void* H, const void* W, int dtype,
 /* Synchronises `stream`, returns the status found on the device by the last call that
  * used `ws` (FCKL_OK if none), and clears it. */
 int fckl_check(void* ws, void* stream);
+
+/* Self-test of failure detection: launches one kernel that waits, with the same bounded
+ * wait the pipeline kernels use but a 50 ms limit, on a barrier nothing arrives at. The wait
+ * gives up, the kernel records a timeout in the status word at the start of ws and returns
+ * normally, so fckl_check(ws, stream) then returns FCKL_ERR_TIMEOUT and the context stays
+ * usable. ws: device buffer of at least 256 bytes (any fckl workspace will do). */
+int fckl_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream);
 
 /* Static text for a status code. */
 const char* fckl_status_string(int status);

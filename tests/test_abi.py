@@ -70,19 +70,21 @@ def test_argument_errors_launch_nothing(fckl):
     p = ctypes.c_void_p(256)  # never dereferenced: the checks fail first
     z = ctypes.c_void_p(0)
     # bad sizes
-    assert lib.fckl_forward(p, p, 0, p, p, 0, 256, 4096, 16, 16, p, p, z, p, 1 << 30, z) == fckl.ERR_ARG
-    assert lib.fckl_forward(p, p, 0, p, p, 64, 250, 4096, 16, 16, p, p, z, p, 1 << 30, z) == fckl.ERR_UNSUPPORTED
+    assert lib.fckl_forward(p, p, 0, p, p, z, 0, 256, 4096, 16, 16, p, p, z, p, 1 << 30, z) == fckl.ERR_ARG
+    assert lib.fckl_forward(p, p, 0, p, p, z, 64, 250, 4096, 16, 16, p, p, z, p, 1 << 30, z) == \
+        fckl.ERR_UNSUPPORTED
     # null input
-    assert lib.fckl_forward(z, p, 0, p, p, 64, 256, 4096, 16, 16, p, p, z, p, 1 << 30, z) == fckl.ERR_ARG
+    assert lib.fckl_forward(z, p, 0, p, p, z, 64, 256, 4096, 16, 16, p, p, z, p, 1 << 30, z) == fckl.ERR_ARG
     # misaligned H
-    assert lib.fckl_forward(ctypes.c_void_p(258), p, 0, p, p, 64, 256, 4096, 16, 16, p, p, z, p, 1 << 30,
+    assert lib.fckl_forward(ctypes.c_void_p(258), p, 0, p, p, z, 64, 256, 4096, 16, 16, p, p, z, p, 1 << 30,
                             z) == fckl.ERR_ARG
     # workspace too small
-    assert lib.fckl_forward(p, p, 0, p, p, 64, 256, 4096, 16, 16, p, p, z, p, 16, z) == fckl.ERR_WORKSPACE
-    assert lib.fckl_backward(p, p, 0, p, p, p, 64, 256, 4096, 16, 16, ctypes.c_float(1.0), p, p, p, 16,
+    assert lib.fckl_forward(p, p, 0, p, p, z, 64, 256, 4096, 16, 16, p, p, z, p, 16, z) == fckl.ERR_WORKSPACE
+    assert lib.fckl_backward(p, p, 0, p, p, z, p, 64, 256, 4096, 16, 16, ctypes.c_float(1.0), p, p, p, 16,
                              z) == fckl.ERR_WORKSPACE
-    assert lib.fckl_backward(p, p, 1, p, p, z, 64, 256, 4096, 16, 16, ctypes.c_float(1.0), p, p, p,
-                             1 << 30, z) in (fckl.ERR_ARG, fckl.ERR_CUDA, fckl.ERR_UNSUPPORTED)
+    assert lib.fckl_forward_backward(p, p, 0, p, p, z, 64, 256, 4096, 16, 16, ctypes.c_float(1.0), p, p, z, p,
+                                     p, p, 16, z) == fckl.ERR_WORKSPACE
+    assert lib.fckl_selftest_wait_timeout(p, 16, z) == fckl.ERR_ARG
     assert lib.fckl_check(z, z) == fckl.ERR_ARG
     assert lib.fckl_launch_count() == before
 

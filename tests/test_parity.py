@@ -71,6 +71,9 @@ def test_tiny_workload_fp32(fckl):
     (130, 384, 2056, 33, 200),    # chunk not a multiple of 128; d = 1.5 N tiles; V % 256 = 8
     (1, 64, 256, 1, 1),           # one position, one slot
     (70, 128, 1000, 20, 1000),    # chunk larger than N
+    (40, 8, 16, 16, 16),          # smallest d (one partial K block), V below one tile, K = V
+    (96, 64, 2048, 1024, 48),     # the largest K the preprocess takes
+    (513, 192, 256, 7, 512),      # one vocabulary tile, chunk = 2 pair tiles; a 1-row tail
 ])
 def test_ragged_shapes_bf16(fckl, N, d, V, K, chunk):
     x = synthetic.make_inputs(N, d, V, K, dtype="bf16", seed=N + d)
@@ -134,3 +137,70 @@ def test_repeat_calls_are_deterministic(fckl):
     assert a[0] == b[0]
     for u, v in zip(a[1:], b[1:]):
         np.testing.assert_array_equal(u, v)
+
+
+def test_position_weights_and_fused_call(fckl):
+    """Weights (0 = padding, fractional, 2) against the oracle; the single forward+backward
+    call gives the same bits as separate forward and backward calls."""
+    N, d, V, K, chunk = 300, 256, 3000, 30, 128
+    x = synthetic.make_inputs(N, d, V, K, dtype="bf16", seed=11)
+    wt = np.ones(N, dtype=np.float32)
+    wt[::7] = 0.0
+    wt[1::5] = 0.5
+    wt[2::11] = 2.0
+    H, W, idx, logp = to_dev(x, "bf16")
+    wd = torch.from_numpy(wt).cuda()
+    ws = fckl.Workspace(N, d, V, K, chunk, fckl.BF16)
+    loss, lse, rl, dH, dW = fckl.forward_backward(H, W, idx, logp, chunk, grad_scale=0.5, ws=ws, weight=wd,
+                                                  row_loss=True)
+    assert fckl.check(ws) == fckl.OK
+    got = (float(loss.item()), lse.cpu().numpy().astype(np.float64), rl.cpu().numpy().astype(np.float64),
+           dH.float().cpu().numpy().astype(np.float64), dW.cpu().numpy().astype(np.float64))
+    r_loss, r_lse, r_rl = orc.forward(x["H"], x["W"], x["idx"], x["logp"], chunk, weight=wt)
+    r_dH, r_dW = orc.backward(x["H"], x["W"], x["idx"], x["logp"], 0.5, chunk, weight=wt)
+    assert abs(got[0] - r_loss) <= LOSS_RTOL * abs(r_loss)
+    assert np.abs(got[1] - r_lse).max() <= 1e-3 * (1 + np.abs(r_lse).max())
+    assert np.abs(got[2] - r_rl).max() <= 1e-3 * (1 + np.abs(r_rl).max())
+    assert np.abs(got[3] - r_dH).max() <= GRAD_TOL * np.abs(r_dH).max()
+    assert np.abs(got[4] - r_dW).max() <= GRAD_TOL * np.abs(r_dW).max()
+    assert np.all(got[3][wt == 0] == 0) and np.all(got[2][wt == 0] == 0)
+
+    loss2, lse2, rl2 = fckl.forward(H, W, idx, logp, chunk, ws=ws, weight=wd, row_loss=True)
+    dH2, dW2 = fckl.backward(H, W, idx, logp, lse2, chunk, grad_scale=0.5, ws=ws, weight=wd)
+    assert fckl.check(ws) == fckl.OK
+    assert float(loss2.item()) == got[0]
+    assert torch.equal(lse2, lse) and torch.equal(rl2, rl)
+    assert torch.equal(dH2, dH) and torch.equal(dW2, dW)
+
+
+def test_autograd_wrapper(fckl):
+    N, d, V, K, chunk = 200, 128, 2048, 20, 64
+    x = synthetic.make_inputs(N, d, V, K, dtype="bf16", seed=12)
+    H, W, idx, logp = to_dev(x, "bf16")
+    H.requires_grad_(True)
+    W.requires_grad_(True)
+    loss = fckl.fused_chunked_kl(H, W, idx, logp, chunk)
+    (loss / N).backward()
+    r_loss, _, _ = orc.forward(x["H"], x["W"], x["idx"], x["logp"], chunk)
+    r_dH, r_dW = orc.backward(x["H"], x["W"], x["idx"], x["logp"], 1.0 / N, chunk)
+    assert abs(float(loss.item()) - r_loss) <= LOSS_RTOL * abs(r_loss)
+    assert H.grad.dtype == torch.bfloat16 and W.grad.dtype == torch.bfloat16
+    gH = H.grad.float().cpu().numpy()
+    gW = W.grad.float().cpu().numpy()
+    assert np.abs(gH - r_dH).max() <= GRAD_TOL * np.abs(r_dH).max()
+    assert np.abs(gW - r_dW).max() <= GRAD_TOL * np.abs(r_dW).max()
+
+
+def test_bounded_wait_times_out_and_context_survives(fckl):
+    """Failure detection without a fault: a wait that nothing satisfies gives up, the status
+    word says so, and the next call on the same context works."""
+    import ctypes
+    lib = fckl.load()
+    ws = fckl.Workspace(64, 64, 256, 4, 64, fckl.BF16)
+    stream = torch.cuda.current_stream()
+    assert lib.fckl_selftest_wait_timeout(ws.ptr, ws.nbytes, ctypes.c_void_p(stream.cuda_stream)) == fckl.OK
+    assert fckl.check(ws, raise_on_error=False) == fckl.ERR_TIMEOUT
+    assert fckl.check(ws, raise_on_error=False) == fckl.OK
+    x = synthetic.make_inputs(64, 64, 256, 4, dtype="bf16", seed=13)
+    got = run_gpu(fckl, x, 64, "bf16")
+    assert_parity(got, x, 64)
