@@ -57,7 +57,7 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = ["teacher_mass", "logits", "log_partition", "row_loss", "logit_grad",
-           "forward", "backward", "forward_backward", "rows"]
+           "forward", "backward", "forward_backward", "rows", "teacher_topk"]
 
 
 def teacher_mass(logp):
@@ -191,3 +191,33 @@ def rows(H, W, idx, logp, which, grad_scale=1.0, weight=None):
     rl = w * row_loss(z, lse, np.asarray(idx)[which], np.asarray(logp)[which])
     G = logit_grad(z, lse, np.asarray(idx)[which], np.asarray(logp)[which]) * (grad_scale * w)[:, None]
     return lse, rl, G @ W64
+
+
+def teacher_topk(Ht, Wt, K, chunk=None):
+    """The offline teacher cache: per position, the K tokens of largest teacher logit and
+    their log-probabilities under the teacher's full softmax, not renormalised over the K.
+
+    "Hugging Face：让知识蒸馏廉价到可大规模运行", paragraph "离线蒸馏": the teacher runs
+    once and the 100 most probable tokens of every position are cached; "Chunkovaná KL
+    strata ...", section "Čo dopĺňajú podrobnejšie experimenty": the truncated distribution
+    is kept without renormalisation. Returns (idx int64 [N, K], logp fp64 [N, K]), each row
+    ordered by logp descending, equal logits by smaller token id.
+    """
+    Ht = np.asarray(Ht)
+    N = Ht.shape[0]
+    V = np.shape(Wt)[0]
+    if not 1 <= K <= V:
+        raise ValueError("need 1 <= K <= V")
+    chunk = N if not chunk else int(chunk)
+    idx = np.empty((N, K), dtype=np.int64)
+    logp = np.empty((N, K))
+    ids = np.arange(V)
+    for s in range(0, N, max(chunk, 1)):
+        e = min(N, s + chunk)
+        z = logits(Ht[s:e], Wt)
+        lse = log_partition(z)
+        for r in range(e - s):
+            order = np.lexsort((ids, -z[r]))[:K]   # primary key -z, then id
+            idx[s + r] = order
+            logp[s + r] = z[r, order] - lse[r]
+    return idx, logp

@@ -300,3 +300,49 @@ def test_weighted_finite_differences():
         Wm[v, j] -= h
         fd = (orc.forward(H, Wp, idx, logp, weight=w)[0] - orc.forward(H, Wm, idx, logp, weight=w)[0]) / (2 * h)
         assert fd == pytest.approx(dW[v, j], rel=1e-6, abs=1e-9)
+
+
+def test_teacher_topk_matches_library_topk():
+    rng = np.random.default_rng(17)
+    Ht = rng.standard_normal((20, 16))
+    Wt = rng.standard_normal((300, 16)) / 4
+    idx, logp = orc.teacher_topk(Ht, Wt, 12, chunk=7)
+    import torch
+    z = torch.tensor(Ht @ Wt.T)
+    vals, ids = torch.topk(z, 12, dim=1, largest=True, sorted=True)
+    np.testing.assert_array_equal(idx, ids.numpy())
+    lq = torch.log_softmax(z, dim=1)
+    np.testing.assert_allclose(logp, torch.gather(lq, 1, ids).numpy(), rtol=1e-13, atol=1e-13)
+
+
+def test_teacher_topk_invariants():
+    rng = np.random.default_rng(18)
+    Ht = rng.standard_normal((9, 8))
+    Wt = rng.standard_normal((40, 8))
+    # K = V: the whole distribution, so the kept probabilities sum to 1
+    idx, logp = orc.teacher_topk(Ht, Wt, 40)
+    assert np.all(np.sort(idx, axis=1) == np.arange(40))
+    np.testing.assert_allclose(scipy.special.logsumexp(logp, axis=1), 0.0, atol=1e-13)
+    # K < V: not renormalised (mass < 1), descending, and nothing left out beats the K-th
+    idx, logp = orc.teacher_topk(Ht, Wt, 6)
+    assert np.all(np.exp(logp).sum(1) < 1.0)
+    assert np.all(np.diff(logp, axis=1) <= 0)
+    lq = scipy.special.log_softmax(Ht @ Wt.T, axis=1)
+    for n in range(9):
+        rest = np.setdiff1d(np.arange(40), idx[n])
+        assert lq[n, rest].max() <= logp[n, -1]
+    # equal logits: the smaller id first
+    Wd = np.repeat(Wt[:5], 2, axis=0)
+    idx, _ = orc.teacher_topk(Ht, Wd, 10)
+    for n in range(9):
+        for a, b in zip(idx[n][0::2], idx[n][1::2]):
+            assert a // 2 == b // 2 and a < b
+
+
+def test_cache_built_from_the_student_gives_zero_loss():
+    """A cache built by the teacher-side routine from the student's own H and W makes the
+    student equal to the teacher on the cached ids: the loss vanishes."""
+    x = _problem(16, 24, 500, 30, seed=19)
+    idx, logp = orc.teacher_topk(x["H"], x["W"], 30)
+    loss, _, rl = orc.forward(x["H"], x["W"], idx, logp)
+    assert np.abs(rl).max() < 1e-12
