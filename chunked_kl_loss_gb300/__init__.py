@@ -21,14 +21,14 @@ import ctypes
 import os
 
 __all__ = ["LIB_PATH", "FcklError", "load", "workspace_bytes", "Workspace", "forward", "backward",
-           "forward_backward", "fused_chunked_kl", "check", "launch_count", "profile_enable", "profile_read",
+           "forward_backward", "fused_chunked_kl", "teacher_topk", "check", "launch_count", "profile_enable", "profile_read",
            "kernel_names", "OK", "ERR_ARG", "ERR_INDEX", "ERR_CUDA", "ERR_TIMEOUT",
-           "ERR_WORKSPACE", "ERR_UNSUPPORTED"]
+           "ERR_WORKSPACE", "ERR_UNSUPPORTED", "ERR_CAPACITY"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libfckl.so")
 
-OK, ERR_ARG, ERR_INDEX, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_UNSUPPORTED = range(7)
+OK, ERR_ARG, ERR_INDEX, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CAPACITY = range(8)
 BF16, F32 = 0, 1
 
 _lib = None
@@ -64,6 +64,10 @@ def load():
                                           vp, vp, sz, vp]
     lib.fckl_selftest_wait_timeout.restype = i32
     lib.fckl_selftest_wait_timeout.argtypes = [vp, sz, vp]
+    lib.fckl_topk_workspace_bytes.restype = sz
+    lib.fckl_topk_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
+    lib.fckl_teacher_topk.restype = i32
+    lib.fckl_teacher_topk.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, vp, vp, vp, sz, vp]
     lib.fckl_check.restype = i32
     lib.fckl_check.argtypes = [vp, vp]
     lib.fckl_status_string.restype = c.c_char_p
@@ -106,11 +110,15 @@ def workspace_bytes(N: int, d: int, V: int, K: int, chunk: int, dtype: int = BF1
 
 
 class Workspace:
-    """A device workspace sized for one problem shape (a torch uint8 tensor)."""
+    """A device workspace sized for one problem shape (a torch uint8 tensor); ``kind`` is
+    "loss" (forward/backward) or "topk" (teacher cache builder)."""
 
-    def __init__(self, N, d, V, K, chunk, dtype=BF16, device=None):
+    def __init__(self, N, d, V, K, chunk, dtype=BF16, device=None, kind="loss"):
         import torch
-        n = workspace_bytes(N, d, V, K, chunk, dtype)
+        if kind == "topk":
+            n = int(load().fckl_topk_workspace_bytes(N, d, V, K, chunk, dtype))
+        else:
+            n = workspace_bytes(N, d, V, K, chunk, dtype)
         if n == 0:
             raise FcklError(ERR_UNSUPPORTED, "workspace_bytes")
         self.nbytes = n
@@ -257,6 +265,34 @@ def fused_chunked_kl(H, W, idx, logp, chunk, weight=None):
     if _FusedChunkedKL is None:
         _FusedChunkedKL = _autograd_function()
     return _FusedChunkedKL.apply(H, W, idx, logp, chunk, weight)
+
+
+def teacher_topk(Ht, Wt, K, chunk, ws=None, stream=None):
+    """Offline teacher cache: (idx int32 [N, K], logp fp32 [N, K]) — the K tokens of largest
+    teacher logit per position, by logit descending, with full-softmax log-probabilities."""
+    import torch
+    N, d = Ht.shape
+    V = Wt.shape[0]
+    if Wt.shape[1] != d or Ht.dtype != Wt.dtype:
+        raise ValueError("expected Ht [N,d] and Wt [V,d] of one dtype")
+    for t in (Ht, Wt):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    dt = _dtype_code(Ht)
+    global _last_ws
+    import weakref
+    if ws is None:
+        ws = Workspace(N, d, V, K, chunk, dt, Ht.device, kind="topk")
+        _last_ws = ws
+    else:
+        _last_ws = weakref.ref(ws)
+    idx = torch.empty(N, K, dtype=torch.int32, device=Ht.device)
+    logp = torch.empty(N, K, dtype=torch.float32, device=Ht.device)
+    st = load().fckl_teacher_topk(_ptr(Ht), _ptr(Wt), dt, N, d, V, K, chunk, _ptr(idx), _ptr(logp), ws.ptr,
+                                  ws.nbytes, _stream_ptr(stream))
+    if st != OK:
+        raise FcklError(st, "fckl_teacher_topk")
+    return idx, logp
 
 
 def check(ws=None, stream=None, raise_on_error=True) -> int:

@@ -40,12 +40,17 @@ enum Kind {
   KIND_BWD_DW,
   KIND_CVT,
   KIND_SELFTEST,
+  KIND_TOPK_LOGITS,
+  KIND_TOPK_THRESHOLD,
+  KIND_TOPK_COLLECT,
+  KIND_TOPK_SELECT,
   KIND_COUNT
 };
 const char* const kKindNames[KIND_COUNT] = {"preprocess",     "fwd_logits_lse", "fwd_combine",
                                             "loss_reduce",    "bwd_logit_grad", "bwd_dH_gemm",
                                             "bwd_dH_reduce",  "bwd_dW_gemm",    "cvt_bf16",
-                                            "wait_timeout_selftest"};
+                                            "wait_timeout_selftest", "topk_logits_stats", "topk_threshold",
+                                            "topk_collect",           "topk_select"};
 
 // ------------------------------------------------------------------ process state
 std::mutex g_mu;
@@ -574,6 +579,43 @@ int run_setup(Run& r, const void* H, const void* W, int dtype, const int32_t* id
   return FCKL_OK;
 }
 
+// ------------------------------------------------------------------ teacher top-K cache builder
+constexpr int TOPK_CAND_MAX = 2048;  // candidate slots per position when K <= vocabulary tiles
+
+struct TopkPlan {
+  int chunk, rows_alloc, tiles_v, cmax;
+  size_t off_status, off_pm, off_pl, off_pc, off_lse, off_thr, off_cnt, off_cv, off_cz, off_Hb, off_Wb, total;
+};
+
+TopkPlan make_topk_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
+  TopkPlan p{};
+  p.chunk = static_cast<int>(std::min<int64_t>(chunk, N));
+  p.rows_alloc = static_cast<int>(rup(p.chunk, 256));
+  p.tiles_v = static_cast<int>(cdiv(V, VOCAB_TILE));
+  // With fewer vocabulary tiles than K the threshold is -inf and every token is a candidate.
+  p.cmax = K > p.tiles_v ? V : std::min(V, TOPK_CAND_MAX);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t r = o;
+    o = static_cast<size_t>(rup(static_cast<int64_t>(o + bytes), 1024));
+    return r;
+  };
+  const size_t R = p.rows_alloc;
+  p.off_status = take(256);
+  p.off_pm = take(static_cast<size_t>(p.tiles_v) * R * 4);
+  p.off_pl = take(static_cast<size_t>(p.tiles_v) * R * 4);
+  p.off_pc = take(static_cast<size_t>(p.tiles_v) * R * 4);
+  p.off_lse = take(R * 4);
+  p.off_thr = take(R * 4);
+  p.off_cnt = take(R * 4);
+  p.off_cv = take(R * p.cmax * 4);
+  p.off_cz = take(R * p.cmax * 4);
+  p.off_Hb = dt == FCKL_F32 ? take(R * d * 2) : o;
+  p.off_Wb = dt == FCKL_F32 ? take(static_cast<size_t>(V) * d * 2) : o;
+  p.total = o;
+  return p;
+}
+
 }  // namespace
 }  // namespace fckl
 
@@ -668,6 +710,96 @@ int fckl_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream) {
                 [&] { wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(status, 50000000ull); });
 }
 
+size_t fckl_topk_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype) {
+  if (check_shape(N, d, V, K, chunk, dtype) != FCKL_OK) return 0;
+  return make_topk_plan(N, d, V, K, chunk, dtype).total;
+}
+
+int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int d, int V, int K, int chunk,
+                      int32_t* idx, float* logp, void* ws, size_t ws_bytes, void* stream) {
+  int st = check_shape(N, d, V, K, chunk, dtype);
+  if (st) return st;
+  if (!Ht || !Wt || !idx || !logp || !ws) return FCKL_ERR_ARG;
+  if (!aligned(Ht, 16) || !aligned(Wt, 16) || !aligned(ws, 256) || !aligned(idx, 4) || !aligned(logp, 4))
+    return FCKL_ERR_ARG;
+  const TopkPlan tp = make_topk_plan(N, d, V, K, chunk, dtype);
+  if (ws_bytes < tp.total) return FCKL_ERR_WORKSPACE;
+  DevInfo* di = nullptr;
+  if ((st = device_info(&di))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  unsigned* status = reinterpret_cast<unsigned*>(w + tp.off_status);
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) {
+    set_error("cudaMemsetAsync", e);
+    return FCKL_ERR_CUDA;
+  }
+  const void* Wb = Wt;
+  if (dtype == FCKL_F32) {
+    if ((st = launch_cvt(static_cast<const float*>(Wt), w + tp.off_Wb, int64_t(V) * d, di, s))) return st;
+    Wb = w + tp.off_Wb;
+  }
+  CUtensorMap tmW;
+  if ((st = make_map(&tmW, Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK, VOCAB_TILE / CG)))
+    return st;
+  float* pm = reinterpret_cast<float*>(w + tp.off_pm);
+  float* pl = reinterpret_cast<float*>(w + tp.off_pl);
+  float* lse = reinterpret_cast<float*>(w + tp.off_lse);
+  float* thr = reinterpret_cast<float*>(w + tp.off_thr);
+  int* cnt = reinterpret_cast<int*>(w + tp.off_cnt);
+  int* cv = reinterpret_cast<int*>(w + tp.off_cv);
+  float* cz = reinterpret_cast<float*>(w + tp.off_cz);
+  const size_t esz = dtype == FCKL_F32 ? 4 : 2;
+  for (int64_t r0 = 0; r0 < N; r0 += tp.chunk) {
+    const int rows = static_cast<int>(std::min<int64_t>(tp.chunk, N - r0));
+    const void* Hc = static_cast<const uint8_t*>(Ht) + static_cast<size_t>(r0) * d * esz;
+    if (dtype == FCKL_F32) {
+      if ((st = launch_cvt(static_cast<const float*>(Hc), w + tp.off_Hb, int64_t(rows) * d, di, s))) return st;
+      Hc = w + tp.off_Hb;
+    }
+    // pass 1: per (row, vocabulary tile) max and sum-exp
+    TcParams p;
+    memset(&p, 0, sizeof(p));
+    if ((st = make_map(&p.tmA, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM))) return st;
+    p.tmB = tmW;
+    p.sch = {static_cast<int>(cdiv(rows, TILE_M)), tp.tiles_v, static_cast<int>(cdiv(d, BK)), 1,
+             static_cast<int>(cdiv(d, BK)), 1};
+    p.num_units = p.sch.m_blocks * p.sch.n_blocks;
+    p.status = status;
+    p.rows_valid = rows;
+    p.V = V;
+    p.K = 0;  // no cached teacher slots to gather
+    p.pm = pm;
+    p.pl = pl;
+    p.pc = reinterpret_cast<float*>(w + tp.off_pc);
+    p.ld_part = tp.rows_alloc;
+    if ((st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_STATS>(KIND_TOPK_LOGITS, di, p, s, "topk_logits_stats")))
+      return st;
+    const int wblocks = static_cast<int>(cdiv(rows, 4));
+    const int ld = tp.rows_alloc, tiles = tp.tiles_v;
+    if ((st = launch(KIND_TOPK_THRESHOLD, s, "topk_threshold", [&] {
+           topk_threshold_kernel<<<wblocks, 128, 0, s>>>(pm, pl, ld, tiles, rows, K, lse, thr, cnt);
+         })))
+      return st;
+    // pass 2: the logits recomputed; every logit at or above the threshold becomes a candidate
+    p.thr = thr;
+    p.cnt = cnt;
+    p.cand_v = cv;
+    p.cand_z = cz;
+    p.cmax = tp.cmax;
+    if ((st = launch_tc<VOCAB_TILE, false, false, EPI_TOPK_COLLECT>(KIND_TOPK_COLLECT, di, p, s, "topk_collect")))
+      return st;
+    int32_t* io = idx + r0 * K;
+    float* lo = logp + r0 * K;
+    const int cmax = tp.cmax;
+    if ((st = launch(KIND_TOPK_SELECT, s, "topk_select", [&] {
+           topk_select_kernel<<<wblocks, 128, 0, s>>>(cv, cz, cnt, cmax, rows, K, lse, io, lo, status);
+         })))
+      return st;
+  }
+  return FCKL_OK;
+}
+
 int fckl_check(void* ws, void* stream) {
   if (!ws) return FCKL_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -683,6 +815,7 @@ int fckl_check(void* ws, void* stream) {
   }
   if (word & ST_TIMEOUT) return FCKL_ERR_TIMEOUT;
   if (word & ST_BAD_INDEX) return FCKL_ERR_INDEX;
+  if (word & ST_CAPACITY) return FCKL_ERR_CAPACITY;
   return FCKL_OK;
 }
 
@@ -695,6 +828,7 @@ const char* fckl_status_string(int status) {
     case FCKL_ERR_TIMEOUT: return "a bounded device wait ran out";
     case FCKL_ERR_WORKSPACE: return "workspace smaller than fckl_workspace_bytes()";
     case FCKL_ERR_UNSUPPORTED: return "unsupported shape or device (needs sm_103, d % 8 == 0, K <= min(V, 1024))";
+    case FCKL_ERR_CAPACITY: return "a position had more top-K candidates than the candidate buffer holds";
     default: return "unknown status";
   }
 }

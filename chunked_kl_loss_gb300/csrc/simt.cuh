@@ -109,6 +109,95 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   }
 }
 
+// Teacher cache builder, between the two passes over the vocabulary. One warp per position:
+// lse_n from the per-tile (max, sum-exp) statistics, and the threshold thr_n = the K-th
+// largest of the per-tile maxima (-inf when there are fewer tiles than K). The K largest tile
+// maxima are K distinct logits of the row, so the row's K-th largest logit is >= thr_n and every
+// top-K entry is at or above it. Also clears the row's candidate counter.
+__global__ void __launch_bounds__(128) topk_threshold_kernel(const float* __restrict__ pm,
+                                                             const float* __restrict__ pl, int ld, int tiles,
+                                                             int rows, int K, float* __restrict__ lse_out,
+                                                             float* __restrict__ thr_out, int* __restrict__ cnt) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + warp;
+  if (row >= rows) return;  // warp-uniform
+  float M = -INFINITY, Lr = 0.f;
+  for (int t = lane; t < tiles; t += 32) {
+    const float m = pm[static_cast<size_t>(t) * ld + row], l = pl[static_cast<size_t>(t) * ld + row];
+    const float nm = fmaxf(M, m);
+    Lr = Lr * expf(M - nm) + l * expf(m - nm);
+    M = nm;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, M, o), l2 = __shfl_xor_sync(0xffffffffu, Lr, o);
+    const float nm = fmaxf(M, m2);
+    Lr = (M == -INFINITY ? 0.f : Lr * expf(M - nm)) + (m2 == -INFINITY ? 0.f : l2 * expf(m2 - nm));
+    M = nm;
+  }
+  float thr = -INFINITY;
+  if (K <= tiles) {
+    // K-th largest of the tile maxima: bitwise search on an order-preserving integer key.
+    uint32_t prefix = 0;
+    for (int bit = 31; bit >= 0; --bit) {
+      const uint32_t cand = prefix | (1u << bit);
+      int c = 0;
+      for (int t = lane; t < tiles; t += 32) {
+        const uint32_t u = __float_as_uint(pm[static_cast<size_t>(t) * ld + row]);
+        const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+        c += key >= cand;
+      }
+      c = __reduce_add_sync(0xffffffffu, c);
+      if (c >= K) prefix = cand;
+    }
+    const uint32_t u = (prefix & 0x80000000u) ? (prefix & 0x7FFFFFFFu) : ~prefix;
+    thr = __uint_as_float(u);
+  }
+  if (lane == 0) {
+    lse_out[row] = M + logf(Lr);
+    thr_out[row] = thr;
+    cnt[row] = 0;
+  }
+}
+
+// Teacher cache builder, last step. One warp per position: ranks the row's candidates by
+// (logit descending, token id ascending) and writes the first K as (id, logit - lse).
+// A row with more candidates than the buffer holds raises ST_CAPACITY (its output is then
+// not the exact top-K).
+__global__ void __launch_bounds__(128) topk_select_kernel(const int* __restrict__ cand_v,
+                                                          const float* __restrict__ cand_z,
+                                                          const int* __restrict__ cnt, int cmax, int rows, int K,
+                                                          const float* __restrict__ lse,
+                                                          int32_t* __restrict__ idx_out,
+                                                          float* __restrict__ logp_out,
+                                                          unsigned* __restrict__ status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + warp;
+  if (row >= rows) return;  // warp-uniform
+  int c = cnt[row];
+  if (c > cmax) {
+    if (lane == 0) atomicOr(status, ST_CAPACITY);
+    c = cmax;
+  }
+  const int* cv = cand_v + static_cast<size_t>(row) * cmax;
+  const float* cz = cand_z + static_cast<size_t>(row) * cmax;
+  const float l = lse[row];
+  for (int i = lane; i < c; i += 32) {
+    const float zi = cz[i];
+    const int vi = cv[i];
+    int r = 0;
+    for (int j = 0; j < c; ++j) {
+      const float zj = cz[j];
+      const int vj = cv[j];
+      r += (zj > zi) | ((zj == zi) & (vj < vi));
+    }
+    if (r < K) {
+      idx_out[static_cast<size_t>(row) * K + r] = vi;
+      logp_out[static_cast<size_t>(row) * K + r] = zi - l;
+    }
+  }
+}
+
 // Sum of the per-position losses in a fixed order, in fp64.
 __global__ void __launch_bounds__(1024) loss_reduce_kernel(const float* __restrict__ row_loss, int64_t n,
                                                            float* __restrict__ loss) {

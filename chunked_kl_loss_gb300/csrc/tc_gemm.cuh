@@ -20,6 +20,8 @@
 //   EPI_LOGIT_GRAD: G = scale * w_n * (S_n exp(z - lse_n) - p at the cached ids), rounded
 //                   to bf16 and stored with TMA (the backward pass recomputes the chunk)
 //   EPI_STORE_F32 : fp32 tile stored, or reduce-added, with TMA (dH partials, dW)
+//   EPI_TOPK_COLLECT: appends every logit at or above the row's threshold, with its token
+//                   id, to the row's candidate list (teacher top-K cache builder)
 // Every wait is bounded by WAIT_TIMEOUT_NS; on expiry the CTA records FCKL status bit
 // ST_TIMEOUT, lets its copies and MMAs in flight drain, frees TMEM and returns.
 #pragma once
@@ -42,8 +44,8 @@ constexpr uint32_t EPI_BUF_BYTES = 4096;  // 32 rows x 128 B staging box per epi
 constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;
 constexpr float LOG2E = 1.4426950408889634f;
 
-enum : unsigned { ST_BAD_INDEX = 1u, ST_TIMEOUT = 2u };
-enum { EPI_FWD_STATS = 0, EPI_LOGIT_GRAD = 1, EPI_STORE_F32 = 2 };
+enum : unsigned { ST_BAD_INDEX = 1u, ST_TIMEOUT = 2u, ST_CAPACITY = 4u };
+enum { EPI_FWD_STATS = 0, EPI_LOGIT_GRAD = 1, EPI_STORE_F32 = 2, EPI_TOPK_COLLECT = 3 };
 
 struct Sched {
   int m_blocks, n_blocks, k_blocks;
@@ -76,6 +78,12 @@ struct TcParams {
   int c_reduce;      // 1: reduce-add into tmC, 0: plain store
   int c_xlim, c_ylim;  // extent of tmC: boxes starting at or past it are not issued
   int c_prefetch;      // 1: prefetch each unit's output tile into L2 when its loads start
+  // top-K candidate collection (teacher cache builder)
+  const float* thr;  // [rows] logits at or above it are candidates
+  int* cnt;          // [rows] candidates found (may exceed cmax)
+  int* cand_v;       // [rows][cmax] token ids
+  float* cand_z;     // [rows][cmax] logits
+  int cmax;
 };
 
 // Shared-memory layout of one CTA. CG = CTAs per MMA (1: a 128 x BN tile per CTA; 2: a
@@ -497,6 +505,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
               const int sx = v0 + 64 * jj;
               if (sx < p.c_xlim && row0 < p.c_ylim) tma_store_2d(&p.tmC, buf, sx, row0);
               bulk_commit();
+            }
+          }
+        }
+      } else if constexpr (EPI == EPI_TOPK_COLLECT) {
+        const bool valid = row < p.rows_valid;
+        const float th = valid ? __ldg(p.thr + row) : INFINITY;
+        const int v0 = nb * BN;
+        int* cv = p.cand_v + static_cast<size_t>(valid ? row : 0) * p.cmax;
+        float* cz = p.cand_z + static_cast<size_t>(valid ? row : 0) * p.cmax;
+        if (!warp_wait_phase(&tfull[acc], use & 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int j = 0; j < BN / 32; ++j) {
+          float x[32];
+          __syncwarp();
+          tmem_ld32(taddr + 32 * j, x);
+          if (j == BN / 32 - 1) release_acc(acc);
+          const int cb = v0 + 32 * j;
+          uint32_t hits = 0;
+#pragma unroll
+          for (int t = 0; t < 32; ++t) hits |= (x[t] >= th && cb + t < p.V) ? (1u << t) : 0u;
+          while (hits) {
+            const int t = __ffs(hits) - 1;
+            hits &= hits - 1;
+            const int pos = atomicAdd(p.cnt + row, 1);
+            if (pos < p.cmax) {
+              cv[pos] = cb + t;
+              cz[pos] = pick32(x, t);
             }
           }
         }

@@ -58,7 +58,9 @@ typedef enum {
     FCKL_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed; see fckl_last_error() */
     FCKL_ERR_TIMEOUT = 4,     /* a bounded device wait ran out (device-detected) */
     FCKL_ERR_WORKSPACE = 5,   /* ws_bytes below fckl_workspace_bytes() */
-    FCKL_ERR_UNSUPPORTED = 6  /* shape outside the limits above, or not an sm_103 device */
+    FCKL_ERR_UNSUPPORTED = 6, /* shape outside the limits above, or not an sm_103 device */
+    FCKL_ERR_CAPACITY = 7     /* teacher top-K: a position had more candidates than the buffer
+                                 holds (device-detected; that position's output is not exact) */
 } fckl_status;
 
 typedef enum { FCKL_BF16 = 0, FCKL_F32 = 1 } fckl_dtype;
@@ -135,6 +137,26 @@ int fckl_forward_static(const void* H, const void* W, int dtype,
                         int64_t N, int d, int V, int K, int chunk,
                         float* loss, float* lse, float* row_loss,
                         uint32_t* status, void* stream);
+
+/* Offline teacher top-K cache ("Hugging Face：让知识蒸馏廉价到可大规模运行", paragraph "离线蒸馏":
+ * the teacher runs once and the 100 most probable tokens of every position are cached;
+ * "Chunkovaná KL strata ...", section "Čo dopĺňajú podrobnejšie experimenty": kept without
+ * renormalisation). For every position n of the teacher hidden states Ht [N, d] and output
+ * matrix Wt [V, d] (dtype as for the loss), writes the K token ids of largest logit
+ * z_nv = Wt_v . h_n and their log-probabilities under the full softmax, z_nv - lse_n:
+ *   idx  : device int32 [N, K], each row ordered by logit descending, equal logits by smaller id
+ *   logp : device fp32  [N, K]
+ * The logits are projected twice per chunk and never stored: the first pass keeps each row's
+ * per-tile maxima and sum-exp (giving lse_n and a threshold, the K-th largest tile maximum,
+ * that every top-K logit reaches); the second keeps the logits at or above the threshold as
+ * candidates, which are then ranked exactly. A row with more candidates than the buffer holds
+ * (min(V, 2048) slots, or V when K exceeds ceil(V/256)) is reported as FCKL_ERR_CAPACITY by
+ * fckl_check. The workspace is sized by fckl_topk_workspace_bytes. */
+size_t fckl_topk_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
+int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype,
+                      int64_t N, int d, int V, int K, int chunk,
+                      int32_t* idx, float* logp,
+                      void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronises `stream`, returns the status found on the device by the last call that
  * used `ws` (FCKL_OK if none), and clears it. */

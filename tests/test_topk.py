@@ -1,0 +1,115 @@
+"""GPU parity of the teacher top-K cache builder against the fp64 oracle.
+
+Where two logits are closer than the fp32 products can resolve, either token is a correct
+K-th entry, so the comparison takes what is unique and checks the rest for validity:
+  * every row's K log-probabilities, sorted, match the oracle's (max-abs <= 1e-3);
+  * every returned id is distinct, in range, and its log-probability matches the oracle's
+    log-softmax at that id (max-abs <= 1e-3);
+  * an id returned by one side but not the other lies within 1e-3 of the oracle's K-th logit;
+  * rows are ordered by log-probability, and exactly tied logits (duplicated rows of Wt)
+    come out smaller id first, as the oracle orders them.
+"""
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import synthetic
+from oracle import fckl_oracle as orc
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-3
+
+
+def run_topk(fckl, Ht, Wt, K, chunk, dtype="bf16"):
+    dev = torch.device("cuda")
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    H = torch.from_numpy(np.ascontiguousarray(Ht, dtype=np.float32)).to(dev).to(tdt)
+    W = torch.from_numpy(np.ascontiguousarray(Wt, dtype=np.float32)).to(dev).to(tdt)
+    ws = fckl.Workspace(H.shape[0], H.shape[1], W.shape[0], K, chunk, fckl.BF16 if dtype == "bf16" else fckl.F32,
+                        kind="topk")
+    idx, logp = fckl.teacher_topk(H, W, K, chunk, ws=ws)
+    assert fckl.check(ws) == fckl.OK
+    return idx.cpu().numpy().astype(np.int64), logp.cpu().numpy().astype(np.float64)
+
+
+def assert_topk_parity(idx, logp, Ht, Wt, K):
+    V = np.shape(Wt)[0]
+    r_idx, r_logp = orc.teacher_topk(Ht, Wt, K)
+    lq = scipy.special.log_softmax(orc.logits(Ht, Wt), axis=1)
+    assert idx.shape == r_idx.shape
+    assert idx.min() >= 0 and idx.max() < V
+    for n in range(idx.shape[0]):
+        assert len(set(idx[n].tolist())) == K
+    assert np.abs(np.sort(logp, axis=1) - np.sort(r_logp, axis=1)).max() <= TOL
+    assert np.abs(logp - np.take_along_axis(lq, idx, axis=1)).max() <= TOL
+    assert np.all(np.diff(logp, axis=1) <= TOL)
+    kth = r_logp[:, -1]
+    for n in range(idx.shape[0]):
+        g, o = set(idx[n].tolist()), set(r_idx[n].tolist())
+        for v in g ^ o:
+            assert abs(lq[n, v] - kth[n]) <= TOL, (n, v)
+    return r_idx
+
+
+@pytest.mark.parametrize("N,d,V,K,chunk", [
+    (300, 256, 5000, 40, 128),   # ragged chunk and vocabulary tails
+    (64, 128, 1000, 20, 64),     # fewer vocabulary tiles (4) than K: every token a candidate
+    (130, 320, 2056, 100, 200),  # K = 100 over 9 tiles; d not a multiple of 64
+])
+def test_topk_small(fckl, N, d, V, K, chunk):
+    rng = np.random.default_rng(N + V)
+    Ht = synthetic.round_bf16(rng.standard_normal((N, d), dtype=np.float32))
+    Wt = synthetic.round_bf16(rng.standard_normal((V, d), dtype=np.float32) * 3.0 / np.sqrt(d))
+    idx, logp = run_topk(fckl, Ht, Wt, K, chunk)
+    assert_topk_parity(idx, logp, Ht, Wt, K)
+
+
+def test_topk_llama_vocab(fckl):
+    """K = 100 over V = 128256 at d = 3072 (the cache of the 8K-256K workloads)."""
+    x = synthetic.make_inputs(192, 3072, 128256, 1, dtype="bf16", seed=21)
+    idx, logp = run_topk(fckl, x["H"], x["W"], 100, 128)
+    assert_topk_parity(idx, logp, x["H"], x["W"], 100)
+
+
+def test_topk_exact_ties_take_the_smaller_id(fckl):
+    rng = np.random.default_rng(22)
+    Ht = synthetic.round_bf16(rng.standard_normal((50, 64), dtype=np.float32))
+    base = synthetic.round_bf16(rng.standard_normal((600, 64), dtype=np.float32) / 8)
+    Wt = np.repeat(base, 2, axis=0)          # tokens 2i and 2i+1 have identical logits
+    idx, logp = run_topk(fckl, Ht, Wt, 30, 64)
+    r_idx = assert_topk_parity(idx, logp, Ht, Wt, 30)
+    # tied pairs are adjacent, smaller id first, and a pair cut by K keeps its smaller id
+    for n in range(50):
+        for k in range(30):
+            if idx[n, k] % 2 == 1:
+                assert k > 0 and idx[n, k - 1] == idx[n, k] - 1
+
+
+def test_topk_fp32_inputs_and_round_trip(fckl):
+    """fp32 teacher inputs; and a cache built from the student's own H and W gives a loss of
+    (almost) zero through the loss path."""
+    w = synthetic.WORKLOADS["tiny_n64_d256_v4096"]
+    x = synthetic.make_inputs(w.N, w.d, w.V, w.K, dtype="f32", seed=23)
+    idx, logp = run_topk(fckl, x["H"], x["W"], w.K, w.chunk, dtype="f32")
+    xb = dict(x)
+    xb["H"] = synthetic.round_bf16(x["H"])
+    xb["W"] = synthetic.round_bf16(x["W"])
+    assert_topk_parity(idx, logp, xb["H"], xb["W"], w.K)
+    dev = torch.device("cuda")
+    H = torch.from_numpy(x["H"]).to(dev)
+    W = torch.from_numpy(x["W"]).to(dev)
+    loss, _, rl = fckl.forward(H, W, torch.from_numpy(idx.astype(np.int32)).to(dev),
+                               torch.from_numpy(logp.astype(np.float32)).to(dev), w.chunk, row_loss=True)
+    fckl.check()
+    assert np.abs(rl.cpu().numpy()).max() < 1e-4
+
+
+def test_topk_is_deterministic(fckl):
+    rng = np.random.default_rng(24)
+    Ht = synthetic.round_bf16(rng.standard_normal((200, 128), dtype=np.float32))
+    Wt = synthetic.round_bf16(rng.standard_normal((3000, 128), dtype=np.float32) / 4)
+    a = run_topk(fckl, Ht, Wt, 50, 100)
+    b = run_topk(fckl, Ht, Wt, 50, 100)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
