@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--memory-sweep", action="store_true",
                     help="peak device memory of one forward+backward at N = W.N/8, W.N/4, W.N/2, W.N "
                          "(default workload n262144_d3072_v128256), with a linear fit")
+    ap.add_argument("--topk", action="store_true",
+                    help="time the teacher top-K cache builder (fckl_teacher_topk) on the workload's shapes")
     ap.add_argument("--api", default="fused", choices=["fused", "separate"],
                     help="one fckl_forward_backward call per step, or fckl_forward then fckl_backward")
     ap.add_argument("--no-e2e", action="store_true")
@@ -442,8 +444,58 @@ def memory_sweep(args):
     return line
 
 
+def topk_bench(args):
+    """Teacher top-K cache build over the workload: teacher hidden states and output matrix
+    with the shapes (and generators) of H and W, K cached tokens per position."""
+    import torch
+    import chunked_kl_loss_gb300 as fckl
+    fckl.load()
+    w = synthetic.WORKLOADS[args.workload]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    Ht = torch.from_numpy(synthetic.hidden_states(w.N, w.d, args.seed + 10)).to(dev).to(torch.bfloat16)
+    Wt = torch.from_numpy(synthetic.output_projection(w.V, w.d, args.seed + 11)).to(dev).to(torch.bfloat16)
+    ws = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, fckl.BF16, dev, kind="topk")
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        fckl.teacher_topk(Ht, Wt, w.K, w.chunk, ws=ws, stream=stream)
+    fckl.check(ws)
+    torch.cuda.synchronize(dev)
+    fckl.profile_enable(True)
+    fckl.profile_read()
+    n0 = fckl.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        fckl.teacher_topk(Ht, Wt, w.K, w.chunk, ws=ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    prof = fckl.profile_read()
+    fckl.profile_enable(False)
+    fckl.check(ws)
+    peaks, src = measured_peaks()
+    peak = peak_value(peaks, "bf16_tflops_sustained")
+    kname, (kms, kn) = max(prof.items(), key=lambda kv: kv[1][0])
+    fl = 2.0 * w.N * w.d * w.V * args.steps / kn
+    line = {"metric": "teacher top-K cache build positions/s (two projections, 4NdV)", "value": w.N / (ms / 1e3),
+            "unit": UNIT, "ms_per_step": ms, "steps": args.steps, "warmup": args.warmup,
+            "tflops": 4.0 * w.N * w.d * w.V / (ms / 1e3) / 1e12, "dtype": "bf16",
+            "config": config_of(w, "teacher_topk"), "gpu_launches": fckl.launch_count() - n0,
+            "roofline": {"kernel": kname, "bound": "tensor", "achieved": fl / (kms / kn / 1e3) / 1e12,
+                         "peak": peak, "unit": "TFLOP/s", "frac": fl / (kms / kn / 1e3) / 1e12 / peak,
+                         "peak_source": f"{src} bf16 sustained"},
+            "kernel_shares": {k: round(v[0] / max(1e-9, sum(u[0] for u in prof.values())), 4)
+                              for k, v in prof.items() if v[1]}}
+    print(json.dumps(line), flush=True)
+    return line
+
+
 def main():
     args = parse()
+    if args.topk:
+        topk_bench(args)
+        return 0
     if args.memory_sweep:
         if args.workload == DEFAULT_WORKLOAD:
             args.workload = "n262144_d3072_v128256"
