@@ -487,6 +487,17 @@ def topk_bench(args):
                          "peak_source": f"{src} bf16 sustained"},
             "kernel_shares": {k: round(v[0] / max(1e-9, sum(u[0] for u in prof.values())), 4)
                               for k, v in prof.items() if v[1]}}
+    if not args.no_cpu_baseline:
+        from oracle import fckl_oracle as orc
+        n = max(8, int(8.0 * 100e9 / (2.0 * w.d * w.V)))  # ~8 s at ~100 GFLOP/s fp64
+        Hs = synthetic.round_bf16(synthetic.hidden_states(n, w.d, args.seed + 10))
+        Ws = synthetic.round_bf16(synthetic.output_projection(w.V, w.d, args.seed + 11))
+        t0 = time.perf_counter()
+        orc.teacher_topk(Hs, Ws, w.K, chunk=w.chunk)
+        t = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": n / t, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                                "sample": f"fp64 oracle top-{w.K} cache of the first {n} of {w.N} positions "
+                                          f"(full V={w.V}, d={w.d}), {t:.1f} s"}
     print(json.dumps(line), flush=True)
     return line
 
