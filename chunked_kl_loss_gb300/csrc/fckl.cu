@@ -54,6 +54,7 @@ const char* const kKindNames[KIND_COUNT] = {"preprocess",     "fwd_logits_lse", 
 
 // ------------------------------------------------------------------ process state
 std::mutex g_mu;
+std::mutex g_setup_mu;  // serialises one-time per-device kernel set-up
 char g_last_error[512] = "";
 long long g_launches = 0;
 bool g_prof = false;
@@ -103,6 +104,11 @@ int launch(int kind, cudaStream_t s, const char* what, F&& fn) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error(what, e);
+    if (prof) {
+      std::lock_guard<std::mutex> lk(g_mu);
+      g_event_pool.push_back(a);
+      g_event_pool.push_back(b);
+    }
     return FCKL_ERR_CUDA;
   }
   if (prof) cudaEventRecord(b, s);
@@ -285,7 +291,9 @@ int launch_tc(int kind, DevInfo* di, const TcParams& p, cudaStream_t s, const ch
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = CG > 1 ? 1 : 0;
-  if (!attr_done[dev]) {
+  {
+    std::lock_guard<std::mutex> lk(g_setup_mu);  // one-time per-device set-up, any host thread
+    if (!attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) {
       set_error("cudaFuncSetAttribute", e);
@@ -300,6 +308,7 @@ int launch_tc(int kind, DevInfo* di, const TcParams& p, cudaStream_t s, const ch
     }
     max_clusters[dev] = n;
     attr_done[dev] = true;
+    }
   }
   const int clusters = static_cast<int>(std::min<int64_t>(p.num_units, max_clusters[dev]));
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG));
@@ -318,6 +327,7 @@ int launch_preprocess(const Plan& pl, const int32_t* idx, const float* logp, int
   const int blocks = static_cast<int>(cdiv(rows, PRE_WARPS));
   const size_t smem = static_cast<size_t>(PRE_WARPS) * pl.K * 8;
   if (smem > 48 * 1024) {
+    std::lock_guard<std::mutex> lk(g_setup_mu);
     if (!di->pre_attr_done) {
       cudaError_t e = cudaFuncSetAttribute(preprocess_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(PRE_WARPS * K_LIMIT * 8));
