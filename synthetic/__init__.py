@@ -22,8 +22,10 @@ No dataset, model or teacher is available, so every tensor is synthetic:
 * ``H ~ N(0, 1)`` and ``W ~ N(0, 1/d)``, drawn in fp32; for bf16 workloads they
   are then rounded to bf16 (round to nearest even) and the oracle receives the
   rounded values, widened exactly.
-* teacher, per row: K distinct token ids drawn uniformly from ``[0, V)`` (a row
-  with a repeated id is drawn again whole; ids stay in draw order, unsorted),
+* teacher, per row: K distinct token ids drawn uniformly from ``[0, V)``, ids in
+  draw order, unsorted. When K*K <= V all rows are drawn with replacement and a row
+  with a repeated id is drawn again whole (rare by the birthday bound); otherwise
+  each row is drawn without replacement,
   scores ``t ~ N(0, 2^2)`` sorted descending, a kept mass ``S ~ U(0.85, 0.99)``
   and ``logp = log(S * softmax(t))`` computed in fp64 and stored as fp32.
 
@@ -99,14 +101,17 @@ def teacher_cache(N: int, V: int, K: int, seed: int,
     if K > V:
         raise ValueError("K must not exceed V")
     rng = _rng(seed)
-    idx = rng.integers(0, V, size=(N, K), dtype=np.int64)
-    while True:
-        s = np.sort(idx, axis=1)
-        dup = (s[:, 1:] == s[:, :-1]).any(axis=1) if K > 1 else np.zeros(N, bool)
-        n_dup = int(dup.sum())
-        if n_dup == 0:
-            break
-        idx[dup] = rng.integers(0, V, size=(n_dup, K), dtype=np.int64)
+    if K * K <= V:
+        idx = rng.integers(0, V, size=(N, K), dtype=np.int64)
+        while True:
+            s = np.sort(idx, axis=1)
+            dup = (s[:, 1:] == s[:, :-1]).any(axis=1) if K > 1 else np.zeros(N, bool)
+            n_dup = int(dup.sum())
+            if n_dup == 0:
+                break
+            idx[dup] = rng.integers(0, V, size=(n_dup, K), dtype=np.int64)
+    else:
+        idx = np.stack([rng.choice(V, size=K, replace=False) for _ in range(N)]).astype(np.int64)
     t = rng.standard_normal((N, K)) * 2.0
     t = -np.sort(-t, axis=1)
     S = rng.uniform(s_lo, s_hi, size=(N, 1))

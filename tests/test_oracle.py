@@ -346,3 +346,12 @@ def test_cache_built_from_the_student_gives_zero_loss():
     idx, logp = orc.teacher_topk(x["H"], x["W"], 30)
     loss, _, rl = orc.forward(x["H"], x["W"], idx, logp)
     assert np.abs(rl).max() < 1e-12
+
+
+def test_teacher_generator_terminates_when_K_is_close_to_V():
+    import time
+    t0 = time.time()
+    for N, V, K in [(40, 16, 16), (96, 2048, 1024), (513, 256, 7), (8, 100, 99)]:
+        idx, logp = synthetic.teacher_cache(N, V, K, seed=1)
+        assert all(len(set(r)) == K for r in idx.tolist()) and idx.max() < V
+    assert time.time() - t0 < 10
