@@ -80,13 +80,26 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const bool valid = row < rows;
   float M = -INFINITY, Lr = 0.f, C = 0.f;
   if (valid) {
-    for (int t = w; t < tiles; t += 8) {
-      const size_t o = static_cast<size_t>(t) * ld + row;
-      const float m = pm[o], l = pl[o];
-      const float nm = fmaxf(M, m);
-      Lr = Lr * expf(M - nm) + l * expf(m - nm);
-      M = nm;
-      C += pc[o];
+    // Batches of 8 tiles: the 24 loads of a batch are issued before any of them is merged.
+    constexpr int B = 8;
+    for (int t0 = w; t0 < tiles; t0 += 8 * B) {
+      float m[B], l[B], c[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const int t = t0 + 8 * b;
+        const size_t o = static_cast<size_t>(t < tiles ? t : 0) * ld + row;
+        m[b] = t < tiles ? pm[o] : -INFINITY;
+        l[b] = t < tiles ? pl[o] : 0.f;
+        c[b] = t < tiles ? pc[o] : 0.f;
+      }
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        if (m[b] == -INFINITY) continue;
+        const float nm = fmaxf(M, m[b]);
+        Lr = Lr * expf(M - nm) + l[b] * expf(m[b] - nm);
+        M = nm;
+        C += c[b];
+      }
     }
   }
   sm[w][lane] = M;
