@@ -591,9 +591,11 @@ int run_setup(Run& r, const void* H, const void* W, int dtype, const int32_t* id
 
 // ------------------------------------------------------------------ teacher top-K cache builder
 constexpr int TOPK_CAND_MAX = 2048;  // candidate slots per position when K <= vocabulary tiles
+constexpr size_t TOPK_THR_SMEM = 160 * 1024;  // shared-memory budget of the threshold kernel
 
 struct TopkPlan {
   int chunk, rows_alloc, tiles_v, cmax;
+  int thr_rows, thr_stride;  // threshold kernel: positions per block, shared-memory row pitch
   size_t off_status, off_pm, off_pl, off_pc, off_lse, off_thr, off_cnt, off_cv, off_cz, off_Hb, off_Wb, total;
 };
 
@@ -604,6 +606,8 @@ TopkPlan make_topk_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
   p.tiles_v = static_cast<int>(cdiv(V, VOCAB_TILE));
   // With fewer vocabulary tiles than K the threshold is -inf and every token is a candidate.
   p.cmax = K > p.tiles_v ? V : std::min(V, TOPK_CAND_MAX);
+  p.thr_stride = p.tiles_v | 1;  // odd pitch: the lanes of a warp hit distinct banks
+  p.thr_rows = static_cast<size_t>(32) * p.thr_stride * 4 <= TOPK_THR_SMEM ? 32 : 8;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t r = o;
@@ -733,9 +737,23 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
   if (!aligned(Ht, 16) || !aligned(Wt, 16) || !aligned(ws, 256) || !aligned(idx, 4) || !aligned(logp, 4))
     return FCKL_ERR_ARG;
   const TopkPlan tp = make_topk_plan(N, d, V, K, chunk, dtype);
+  if (static_cast<size_t>(tp.thr_rows) * tp.thr_stride * 4 > TOPK_THR_SMEM) return FCKL_ERR_UNSUPPORTED;
   if (ws_bytes < tp.total) return FCKL_ERR_WORKSPACE;
   DevInfo* di = nullptr;
   if ((st = device_info(&di))) return st;
+  {
+    std::lock_guard<std::mutex> lk(g_setup_mu);
+    static bool thr_attr[64] = {};
+    if (!thr_attr[di->id]) {
+      cudaError_t e = cudaFuncSetAttribute(topk_threshold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(TOPK_THR_SMEM));
+      if (e != cudaSuccess) {
+        set_error("cudaFuncSetAttribute(topk_threshold)", e);
+        return FCKL_ERR_CUDA;
+      }
+      thr_attr[di->id] = true;
+    }
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   unsigned* status = reinterpret_cast<unsigned*>(w + tp.off_status);
@@ -787,8 +805,12 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
       return st;
     const int wblocks = static_cast<int>(cdiv(rows, 4));
     const int ld = tp.rows_alloc, tiles = tp.tiles_v;
+    const int tR = tp.thr_rows, tstride = tp.thr_stride;
+    const int tblocks = static_cast<int>(cdiv(rows, tR));
+    const size_t tsmem = static_cast<size_t>(tR) * tstride * 4;
     if ((st = launch(KIND_TOPK_THRESHOLD, s, "topk_threshold", [&] {
-           topk_threshold_kernel<<<wblocks, 128, 0, s>>>(pm, pl, ld, tiles, rows, K, lse, thr, cnt);
+           topk_threshold_kernel<<<tblocks, 256, tsmem, s>>>(pm, pl, ld, tiles, rows, tR, tstride, K, lse, thr,
+                                                             cnt);
          })))
       return st;
     // pass 2: the logits recomputed; every logit at or above the threshold becomes a candidate

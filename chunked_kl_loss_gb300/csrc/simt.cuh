@@ -122,54 +122,74 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   }
 }
 
-// Teacher cache builder, between the two passes over the vocabulary. One warp per position:
-// lse_n from the per-tile (max, sum-exp) statistics, and the threshold thr_n = the K-th
-// largest of the per-tile maxima (-inf when there are fewer tiles than K). The K largest tile
-// maxima are K distinct logits of the row, so the row's K-th largest logit is >= thr_n and every
-// top-K entry is at or above it. Also clears the row's candidate counter.
-__global__ void __launch_bounds__(128) topk_threshold_kernel(const float* __restrict__ pm,
+// Teacher cache builder, between the two passes over the vocabulary. R positions per block
+// (R <= 32), 8 warps: lse_n from the per-tile (max, sum-exp) statistics, and the threshold
+// thr_n = the K-th largest of the per-tile maxima (-inf when there are fewer tiles than K).
+// The K largest tile maxima are K distinct logits of the row, so the row's K-th largest logit
+// is >= thr_n and every top-K entry is at or above it. Also clears the candidate counters.
+// Phase 1 reads the statistics coalesced across the block's rows (lane = row) and stages the
+// maxima, as order-preserving integer keys, in shared memory [R][stride]; phase 2 runs a
+// bitwise search for the K-th largest key, one warp per row.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float order_key_inv(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+__global__ void __launch_bounds__(256) topk_threshold_kernel(const float* __restrict__ pm,
                                                              const float* __restrict__ pl, int ld, int tiles,
-                                                             int rows, int K, float* __restrict__ lse_out,
+                                                             int rows, int R, int stride, int K,
+                                                             float* __restrict__ lse_out,
                                                              float* __restrict__ thr_out, int* __restrict__ cnt) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + warp;
-  if (row >= rows) return;  // warp-uniform
+  extern __shared__ uint32_t keys[];  // [R][stride]
+  __shared__ float sm[8][32], sl[8][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int row = blockIdx.x * R + lane;
+  const bool valid = lane < R && row < rows;
   float M = -INFINITY, Lr = 0.f;
-  for (int t = lane; t < tiles; t += 32) {
-    const float m = pm[static_cast<size_t>(t) * ld + row], l = pl[static_cast<size_t>(t) * ld + row];
-    const float nm = fmaxf(M, m);
-    Lr = Lr * expf(M - nm) + l * expf(m - nm);
-    M = nm;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, M, o), l2 = __shfl_xor_sync(0xffffffffu, Lr, o);
-    const float nm = fmaxf(M, m2);
-    Lr = (M == -INFINITY ? 0.f : Lr * expf(M - nm)) + (m2 == -INFINITY ? 0.f : l2 * expf(m2 - nm));
-    M = nm;
-  }
-  float thr = -INFINITY;
-  if (K <= tiles) {
-    // K-th largest of the tile maxima: bitwise search on an order-preserving integer key.
-    uint32_t prefix = 0;
-    for (int bit = 31; bit >= 0; --bit) {
-      const uint32_t cand = prefix | (1u << bit);
-      int c = 0;
-      for (int t = lane; t < tiles; t += 32) {
-        const uint32_t u = __float_as_uint(pm[static_cast<size_t>(t) * ld + row]);
-        const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-        c += key >= cand;
-      }
-      c = __reduce_add_sync(0xffffffffu, c);
-      if (c >= K) prefix = cand;
+  for (int t = w; t < tiles; t += 8) {
+    if (valid) {
+      const size_t o = static_cast<size_t>(t) * ld + row;
+      const float m = pm[o], l = pl[o];
+      const float nm = fmaxf(M, m);
+      Lr = Lr * expf(M - nm) + l * expf(m - nm);
+      M = nm;
+      keys[lane * stride + t] = order_key(m);
     }
-    const uint32_t u = (prefix & 0x80000000u) ? (prefix & 0x7FFFFFFFu) : ~prefix;
-    thr = __uint_as_float(u);
   }
-  if (lane == 0) {
+  sm[w][lane] = M;
+  sl[w][lane] = Lr;
+  __syncthreads();
+  if (w == 0 && valid) {
+    for (int j = 1; j < 8; ++j) {
+      const float m = sm[j][lane];
+      if (m == -INFINITY) continue;
+      const float nm = fmaxf(M, m);
+      Lr = Lr * expf(M - nm) + sl[j][lane] * expf(m - nm);
+      M = nm;
+    }
     lse_out[row] = M + logf(Lr);
-    thr_out[row] = thr;
     cnt[row] = 0;
+  }
+  for (int r = w; r < R; r += 8) {  // warp-uniform rows
+    const int row2 = blockIdx.x * R + r;
+    if (row2 >= rows) break;
+    float thr = -INFINITY;
+    if (K <= tiles) {
+      const uint32_t* kr = keys + r * stride;
+      uint32_t prefix = 0;
+      for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t cand = prefix | (1u << bit);
+        int c = 0;
+        for (int t = lane; t < tiles; t += 32) c += kr[t] >= cand;
+        c = __reduce_add_sync(0xffffffffu, c);
+        if (c >= K) prefix = cand;
+      }
+      thr = order_key_inv(prefix);
+    }
+    if (lane == 0) thr_out[row2] = thr;
   }
 }
 

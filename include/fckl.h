@@ -151,7 +151,8 @@ int fckl_forward_static(const void* H, const void* W, int dtype,
  * that every top-K logit reaches); the second keeps the logits at or above the threshold as
  * candidates, which are then ranked exactly. A row with more candidates than the buffer holds
  * (min(V, 2048) slots, or V when K exceeds ceil(V/256)) is reported as FCKL_ERR_CAPACITY by
- * fckl_check. The workspace is sized by fckl_topk_workspace_bytes. */
+ * fckl_check. The workspace is sized by fckl_topk_workspace_bytes. V up to 1,310,720
+ * (FCKL_ERR_UNSUPPORTED above). */
 size_t fckl_topk_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
 int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype,
                       int64_t N, int d, int V, int K, int chunk,
