@@ -149,14 +149,26 @@ __global__ void __launch_bounds__(256) topk_threshold_kernel(const float* __rest
   const int row = blockIdx.x * R + lane;
   const bool valid = lane < R && row < rows;
   float M = -INFINITY, Lr = 0.f;
-  for (int t = w; t < tiles; t += 8) {
-    if (valid) {
-      const size_t o = static_cast<size_t>(t) * ld + row;
-      const float m = pm[o], l = pl[o];
-      const float nm = fmaxf(M, m);
-      Lr = Lr * expf(M - nm) + l * expf(m - nm);
-      M = nm;
-      keys[lane * stride + t] = order_key(m);
+  if (valid) {
+    constexpr int B = 8;  // the loads of 8 tiles are issued before any of them is merged
+    for (int t0 = w; t0 < tiles; t0 += 8 * B) {
+      float m[B], l[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const int t = t0 + 8 * b;
+        const size_t o = static_cast<size_t>(t < tiles ? t : 0) * ld + row;
+        m[b] = t < tiles ? pm[o] : -INFINITY;
+        l[b] = t < tiles ? pl[o] : 0.f;
+      }
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const int t = t0 + 8 * b;
+        if (t >= tiles) continue;
+        keys[lane * stride + t] = order_key(m[b]);
+        const float nm = fmaxf(M, m[b]);
+        Lr = Lr * expf(M - nm) + l[b] * expf(m[b] - nm);
+        M = nm;
+      }
     }
   }
   sm[w][lane] = M;
