@@ -607,7 +607,7 @@ TopkPlan make_topk_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
   // With fewer vocabulary tiles than K the threshold is -inf and every token is a candidate.
   p.cmax = K > p.tiles_v ? V : std::min(V, TOPK_CAND_MAX);
   p.thr_stride = p.tiles_v | 1;  // odd pitch: the lanes of a warp hit distinct banks
-  p.thr_rows = static_cast<size_t>(32) * p.thr_stride * 4 <= TOPK_THR_SMEM ? 32 : 8;
+  p.thr_rows = 8;  // 8 positions per block: one per warp in the search, many blocks per chunk
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t r = o;

@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 }
 
 // Teacher cache builder, between the two passes over the vocabulary. R positions per block
-// (R <= 32), 8 warps: lse_n from the per-tile (max, sum-exp) statistics, and the threshold
+// (R <= 8 keeps one position per warp in the search), 8 warps: lse_n from the per-tile (max, sum-exp) statistics, and the threshold
 // thr_n = the K-th largest of the per-tile maxima (-inf when there are fewer tiles than K).
 // The K largest tile maxima are K distinct logits of the row, so the row's K-th largest logit
 // is >= thr_n and every top-K entry is at or above it. Also clears the candidate counters.
