@@ -232,3 +232,13 @@ def test_two_streams_two_workspaces(fckl):
             assert torch.equal(u, v)
         for u, v in zip(ob, ref_b):
             assert torch.equal(u, v)
+
+
+def test_large_logits(fckl):
+    """Logits with standard deviation ~10 (sharp student distributions, as in trained
+    language-model heads): the online max / log-sum-exp and G stay within tolerance."""
+    x = synthetic.make_inputs(300, 256, 5000, 40, dtype="f32", seed=33)
+    x["W"] = synthetic.round_bf16(x["W"] * 10.0)
+    x["H"] = synthetic.round_bf16(x["H"])
+    got = run_gpu(fckl, x, 128, "bf16")
+    assert_parity(got, x, 128)
