@@ -19,7 +19,9 @@
  * Conventions for every call below
  *  - All arrays are dense and row-major. "device" pointers are CUDA device memory of the
  *    current device; the caller owns every buffer, including the workspace. The library
- *    allocates no device memory and keeps only host-side caches (device properties).
+ *    allocates no device memory at run time (the one exception is the fixed scratch array
+ *    of fckl_forward_static, reserved when the library is loaded) and keeps only host-side
+ *    caches (device properties, one-time kernel set-up).
  *  - H is [N, d] and W is [V, d], both of type `dtype` (FCKL_BF16 or FCKL_F32). FCKL_F32
  *    inputs are rounded to bf16 on the device and the tensor-core products run in bf16
  *    with fp32 accumulation, exactly as for FCKL_BF16 inputs.
@@ -65,7 +67,8 @@ typedef enum {
 
 typedef enum { FCKL_BF16 = 0, FCKL_F32 = 1 } fckl_dtype;
 
-/* Bytes of device workspace that fckl_forward and fckl_backward need for this shape.
+/* Bytes of device workspace that fckl_forward, fckl_backward and fckl_forward_backward need
+ * for this shape.
  * The size grows with chunk * V (the gradient slab) and with N only through 4 bytes per
  * position; 0 if the shape is outside the limits. */
 size_t fckl_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
