@@ -377,6 +377,7 @@ def run_ours(args):
                 "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step)",
                 "flops_per_launch": flops_per_launch, "avg_launch_ms": kms / kn}
     shares = {k: round(v[0] / max(1e-9, sum(u[0] for u in prof.values())), 4) for k, v in prof.items() if v[1]}
+    kernel_ms = sum(v[0] for v in prof.values()) / args.steps  # device time of the library's kernels
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -387,6 +388,7 @@ def run_ours(args):
         "gpu_launches": launches,
         "roofline": roof,
         "kernel_shares": shares,
+        "kernel_ms_per_step": kernel_ms,
         "clocks": clk,
         "e2e": e2e,
     }
