@@ -527,7 +527,6 @@ int chunk_backward(Run& r, int64_t r0, int rows, const void* Hc) {
   ph.c_reduce = 0;
   ph.c_xlim = d;
   ph.c_ylim = splits * pl.rows_alloc;
-  ph.n_short_last = d - (nbd - 1) * pl.bn_d <= pl.bn_d / 2 ? 1 : 0;
   if ((st = launch_tc<256, false, true, EPI_STORE_F32>(KIND_BWD_DH, r.di, ph, s, "bwd_dH_gemm"))) return st;
   {
     const int64_t n4 = int64_t(rows) * d / 4;
@@ -562,7 +561,6 @@ int chunk_backward(Run& r, int64_t r0, int rows, const void* Hc) {
   pw.c_prefetch = pw.c_reduce;
   pw.c_xlim = d;
   pw.c_ylim = V;
-  pw.n_short_last = d - (nbd - 1) * pl.bn_d <= pl.bn_d / 2 ? 1 : 0;
   return launch_tc<256, true, true, EPI_STORE_F32>(KIND_BWD_DW, r.di, pw, s, "bwd_dW_gemm");
 }
 

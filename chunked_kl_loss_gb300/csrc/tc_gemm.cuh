@@ -78,7 +78,6 @@ struct TcParams {
   int c_reduce;      // 1: reduce-add into tmC, 0: plain store
   int c_xlim, c_ylim;  // extent of tmC: boxes starting at or past it are not issued
   int c_prefetch;      // 1: prefetch each unit's output tile into L2 when its loads start
-  int n_short_last;    // 1: the last N-tile holds at most BN/2 columns and runs at half width
   // top-K candidate collection (teacher cache builder)
   const float* thr;  // [rows] logits at or above it are candidates
   int* cnt;          // [rows] candidates found (may exceed cmax)
@@ -228,7 +227,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   constexpr int BN_CTA = L::BN_CTA;
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per MMA");
   static_assert(!B_MN || BN_CTA % 64 == 0, "MN-major B is staged in 64-wide blocks");
-  constexpr bool CAN_SHORT = CG == 2 && B_MN && BN == 256;  // half-width last N-tile possible
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
@@ -288,10 +286,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         int mb, nb, sp, kb0, kb1;
         decode_unit(p.sch, u, mb, nb, sp, kb0, kb1);
         const int arow = mb * BM * CG + static_cast<int>(rank) * BM;       // this CTA's A rows
-        // A half-width last N-tile: each CTA stages its 64 columns in the first box; the second
-        // box lies past the matrix (zero fill), which keeps the stage's byte count unchanged.
-        const bool short_t = CAN_SHORT && p.n_short_last && nb == p.sch.n_blocks - 1;
-        const int bcol = nb * BN + static_cast<int>(rank) * (short_t ? 64 : BN_CTA);  // this CTA's B
+        const int bcol = nb * BN + static_cast<int>(rank) * BN_CTA;        // this CTA's B rows/cols
         // A reduce-add epilogue reads its output tile back from memory: start that read now,
         // a whole main loop before the epilogue needs it.
         if (EPI == EPI_STORE_F32 && p.c_prefetch && nb * BN < p.c_xlim && arow < p.c_ylim)
@@ -326,10 +321,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             load(b, &p.tmB, kb * BK, bcol);
           } else {
 #pragma unroll
-            for (int j = 0; j < BN_CTA / 64; ++j)
-              load(b + j * 8192, &p.tmB, (short_t && j > 0) ? nb * BN + BN_CTA + 64 * static_cast<int>(rank)
-                                                            : bcol + 64 * j,
-                   kb * BK);
+            for (int j = 0; j < BN_CTA / 64; ++j) load(b + j * 8192, &p.tmB, bcol + 64 * j, kb * BK);
           }
         }
       }
@@ -348,8 +340,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader CTA)
     if (lane == 0 && leader) {
-      constexpr uint32_t IDESC_FULL = make_idesc_bf16(BM * CG, BN, A_MN, B_MN);
-      constexpr uint32_t IDESC_HALF = make_idesc_bf16(BM * CG, BN / 2, A_MN, B_MN);
+      constexpr uint32_t IDESC = make_idesc_bf16(BM * CG, BN, A_MN, B_MN);
       uint32_t cnt = 0, it = 0;
       bool ok = true;
       for (int u = cluster_id; ok && u < p.num_units; u += num_clusters, ++it) {
@@ -361,8 +352,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         if (!got) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
-        const uint32_t IDESC =
-            (CAN_SHORT && p.n_short_last && nb == p.sch.n_blocks - 1) ? IDESC_HALF : IDESC_FULL;
         for (int kb = kb0; kb < kb1; ++kb, ++cnt) {
           const uint32_t s = cnt % NST, ph = (cnt / NST) & 1u;
           if (!wait_phase(&full[s], ph, abort_flag, p.status)) {
@@ -552,15 +541,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         if (!warp_wait_phase(&tfull[acc], use & 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const int y = sp * p.c_split_rows + row0;
-        const int nsl = (CAN_SHORT && p.n_short_last && nb == p.sch.n_blocks - 1) ? BN / 64 : BN / 32;
 #pragma unroll 1
-        for (int j = 0; j < nsl; ++j, ++ecnt) {
+        for (int j = 0; j < BN / 32; ++j, ++ecnt) {
           uint8_t* buf = ebuf0 + (ecnt & 1u) * EPI_BUF_BYTES;
           if (ecnt >= 2 && lane == 0) bulk_wait_read<1>();
           __syncwarp();
           float x[32];
           tmem_ld32(taddr + 32 * j, x);
-          if (j == nsl - 1) release_acc(acc);
+          if (j == BN / 32 - 1) release_acc(acc);
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) {
             const int chunk16 = cc ^ (lane & 7);
