@@ -259,10 +259,10 @@ def run_ours(args):
     import chunked_kl_loss_gb300 as fckl
 
     rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)  # before the process group: NCCL binds to the current device
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     fckl.load()
     w = synthetic.WORKLOADS[args.workload]
