@@ -3,8 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 One step = one forward + backward over the whole workload (all chunks), inputs resident in
-HBM: one fckl_forward_backward call (--api fused, the default) or fckl_forward then
-fckl_backward (--api separate). Prints one JSON line (rank 0). Under torchrun each rank runs its own
+HBM: one fckl_forward_backward call (--api fused, the default; each chunk's logits kept from
+its forward for its backward, or recomputed with --recompute) or fckl_forward then
+fckl_backward (--api separate, which recomputes). Prints one JSON line (rank 0). Under torchrun each rank runs its own
 replica of the workload (the loss has no exchange step on one GPU: replicas only) and
 the whole-job value is the positions of all ranks over the slowest rank's time.
 
@@ -35,7 +36,7 @@ DEFAULT_WORKLOAD = "n32768_d3072_v128256"
 METRIC = "fused KL fwd+bwd positions/s & TFLOP/s (8NdV) vs BF16 roofline; peak GiB"
 UNIT = "positions/s"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-GEMM_KERNELS = ("fwd_logits_lse", "bwd_logit_grad", "bwd_dH_gemm", "bwd_dW_gemm")
+GEMM_KERNELS = ("fwd_logits_lse", "fwd_logits_keep", "bwd_logit_grad", "bwd_dH_gemm", "bwd_dW_gemm")
 
 
 def parse():
@@ -55,6 +56,9 @@ def parse():
                     help="time the teacher top-K cache builder (fckl_teacher_topk) on the workload's shapes")
     ap.add_argument("--api", default="fused", choices=["fused", "separate"],
                     help="one fckl_forward_backward call per step, or fckl_forward then fckl_backward")
+    ap.add_argument("--recompute", action="store_true",
+                    help="--api fused: recompute each chunk's logits in its backward instead of keeping "
+                         "them from its forward")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -124,7 +128,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": config_of(w, args.api),
+            "config": config_of(w, args.api, args.recompute),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
                              "sample": f"each step: fp64 oracle forward+backward on {n} of {w.N} positions "
                                        f"(full V, d)"},
@@ -133,9 +137,14 @@ def run_reference(args):
     return 0
 
 
-def config_of(w, api="fused"):
+def logits_kept(api, recompute):
+    return api == "fused" and not recompute
+
+
+def config_of(w, api="fused", recompute=False):
     return {"workload": w.name, "N": w.N, "d": w.d, "V": w.V, "K": w.K, "chunk": w.chunk,
             "input_dtype": w.dtype, "parallelism": "replicas", "api": api,
+            "logits": "kept from the forward" if logits_kept(api, recompute) else "recomputed in the backward",
             "l2": "inputs larger than L2 (W alone is %.0f MB)" % (w.V * w.d * 2 / 1e6)}
 
 
@@ -279,14 +288,16 @@ def run_ours(args):
     base_alloc = torch.cuda.memory_allocated(dev)
     H, W, idx, logp = (host[k].to(dev) for k in ("H", "W", "idx", "logp"))
     dt = fckl.BF16 if w.dtype == "bf16" else fckl.F32
-    ws = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, dt, dev)
+    keep = logits_kept(args.api, args.recompute)
+    ws = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, dt, dev, kind="fused" if keep else "loss")
     dH = torch.empty_like(H)
     dW = torch.empty(w.V, w.d, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         if args.api == "fused":
-            loss, _, _, _ = fckl.forward_backward(H, W, idx, logp, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW)
+            loss, _, _, _ = fckl.forward_backward(H, W, idx, logp, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW,
+                                                  keep_logits=keep)
             return loss
         loss, lse = fckl.forward(H, W, idx, logp, w.chunk, ws=ws, stream=stream)
         fckl.backward(H, W, idx, logp, lse, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW)
@@ -334,7 +345,7 @@ def run_ours(args):
             Hd, Wd, idd, lpd = (host[k].to(dev, non_blocking=True) for k in ("H", "W", "idx", "logp"))
             if args.api == "fused":
                 loss, _, _, _ = fckl.forward_backward(Hd, Wd, idd, lpd, w.chunk, ws=ws, stream=stream, dH=dH,
-                                                      dW=dW)
+                                                      dW=dW, keep_logits=keep)
             else:
                 loss, lse = fckl.forward(Hd, Wd, idd, lpd, w.chunk, ws=ws, stream=stream)
                 fckl.backward(Hd, Wd, idd, lpd, lse, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW)
@@ -362,7 +373,9 @@ def run_ours(args):
 
     ms_step = t_max / args.steps
     value = world * w.N * args.steps / (t_max / 1e3)
-    tflops = w.flops() / (ms_step / 1e3) / 1e12
+    tflops = w.flops() / (ms_step / 1e3) / 1e12  # the metric's count: 8NdV, four products
+    products = 3 if keep else 4  # with kept logits the backward's logits product is not run
+    tflops_exec = w.flops() * products / 4 / (ms_step / 1e3) / 1e12
     peaks, peak_src = measured_peaks()
     peak_sus = peak_value(peaks, "bf16_tflops_sustained")
     # dominant kernel: largest share of the measured launch time
@@ -382,8 +395,8 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generators; no dataset)",
-        "config": config_of(w, args.api),
-        "tflops": tflops, "tflops_frac_of_peak": tflops / peak_sus,
+        "config": config_of(w, args.api, args.recompute),
+        "tflops": tflops, "tflops_executed": tflops_exec, "tflops_executed_frac_of_peak": tflops_exec / peak_sus,
         "peak_gib": peak_bytes / 2**30,
         "gpu_launches": launches,
         "roofline": roof,
@@ -421,29 +434,36 @@ def memory_sweep(args):
     W = torch.from_numpy(x["W"]).to(dev).to(torch.bfloat16)
     idx_h, logp_h = torch.from_numpy(x["idx"]), torch.from_numpy(x["logp"])
     del x
-    points = []
-    for n in (w.N // 8, w.N // 4, w.N // 2, w.N):
+    def peak_of(n, fused):
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
         base = torch.cuda.memory_allocated(dev)  # W already resident
         torch.cuda.reset_peak_memory_stats(dev)
         H = Hh[:n].to(dev)
         idx, logp = idx_h[:n].to(dev), logp_h[:n].to(dev)
-        ws = fckl.Workspace(n, w.d, w.V, w.K, w.chunk, fckl.BF16, dev)
-        loss, lse = fckl.forward(H, W, idx, logp, w.chunk, ws=ws)
-        dH, dW = fckl.backward(H, W, idx, logp, lse, w.chunk, ws=ws)
+        ws = fckl.Workspace(n, w.d, w.V, w.K, w.chunk, fckl.BF16, dev, kind="fused" if fused else "loss")
+        if fused:
+            fckl.forward_backward(H, W, idx, logp, w.chunk, ws=ws)
+        else:
+            loss, lse = fckl.forward(H, W, idx, logp, w.chunk, ws=ws)
+            fckl.backward(H, W, idx, logp, lse, w.chunk, ws=ws)
         fckl.check(ws)
-        peak = torch.cuda.max_memory_allocated(dev) - base + W.numel() * 2
-        points.append((n, peak))
-        del H, idx, logp, ws, loss, lse, dH, dW
-    n_arr = np.array([p[0] for p in points], dtype=np.float64)
-    y = np.array([p[1] for p in points], dtype=np.float64)
-    b, a = np.polyfit(n_arr, y, 1)
-    resid = np.abs(y - (a + b * n_arr)) / y
+        return torch.cuda.max_memory_allocated(dev) - base + W.numel() * 2
+
+    def fit(points):
+        n_arr = np.array([p[0] for p in points], dtype=np.float64)
+        y = np.array([p[1] for p in points], dtype=np.float64)
+        b, a = np.polyfit(n_arr, y, 1)
+        resid = np.abs(y - (a + b * n_arr)) / y
+        return {"points": [{"N": int(n), "peak_gib": pk / 2**30} for n, pk in points],
+                "fit_intercept_gib": a / 2**30, "fit_bytes_per_position": b, "max_rel_residual": float(resid.max())}
+
+    sizes = (w.N // 8, w.N // 4, w.N // 2, w.N)
+    sep = fit([(n, peak_of(n, False)) for n in sizes])
+    fused = fit([(n, peak_of(n, True)) for n in sizes])
     line = {"metric": "peak device memory of one forward+backward vs N (GiB)", "workload": w.name,
-            "chunk": w.chunk, "points": [{"N": int(n), "peak_gib": pk / 2**30} for n, pk in points],
-            "fit_intercept_gib": a / 2**30, "fit_bytes_per_position": b,
-            "analytic_bytes_per_position": bytes_per_position(w), "max_rel_residual": float(resid.max())}
+            "chunk": w.chunk, "analytic_bytes_per_position": bytes_per_position(w),
+            "separate_calls_logits_recomputed": sep, "one_call_logits_kept": fused}
     print(json.dumps(line), flush=True)
     return line
 

@@ -44,13 +44,16 @@ enum Kind {
   KIND_TOPK_THRESHOLD,
   KIND_TOPK_COLLECT,
   KIND_TOPK_SELECT,
+  KIND_FWD_LOGITS_KEEP,
+  KIND_BWD_GRAD_KEPT,
   KIND_COUNT
 };
 const char* const kKindNames[KIND_COUNT] = {"preprocess",     "fwd_logits_lse", "fwd_combine",
                                             "loss_reduce",    "bwd_logit_grad", "bwd_dH_gemm",
                                             "bwd_dH_reduce",  "bwd_dW_gemm",    "cvt_bf16",
                                             "wait_timeout_selftest", "topk_logits_stats", "topk_threshold",
-                                            "topk_collect",           "topk_select"};
+                                            "topk_collect",           "topk_select",
+                                            "fwd_logits_keep",        "bwd_grad_from_logits"};
 
 // ------------------------------------------------------------------ process state
 std::mutex g_mu;
@@ -210,6 +213,7 @@ struct Plan {
   int bn_d;        // N-tile of the dH / dW products
   size_t off_status, off_sidx, off_sp, off_S, off_T, off_pm, off_pl, off_pc, off_rowloss, off_G, off_dhp,
       off_Hb, off_Wb, total;
+  size_t off_Z, total_keep;  // the chunk's fp32 logits (row pitch ldG), kept by the one-call path
 };
 
 // N-tile of the dH and dW products (over d). 256 columns: an SM pair stages 128 each, two
@@ -258,6 +262,8 @@ Plan make_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
   p.off_Hb = dt == FCKL_F32 ? take(R * d * 2) : o;
   p.off_Wb = dt == FCKL_F32 ? take(static_cast<size_t>(V) * d * 2) : o;
   p.total = o;
+  p.off_Z = take(R * p.ldG * 4);
+  p.total_keep = o;
   return p;
 }
 
@@ -437,7 +443,8 @@ int chunk_prepare(Run& r, int64_t r0, int rows, const void** Hc) {
 }
 
 // Forward of one chunk: logits tiles -> per-tile (max, sum-exp, gathered sum) -> lse and loss.
-int chunk_forward(Run& r, int64_t r0, int rows, const void* Hc) {
+// With keep, the logits tiles are also stored (fp32) for the chunk's backward.
+int chunk_forward(Run& r, int64_t r0, int rows, const void* Hc, bool keep = false) {
   const Plan& pl = r.pl;
   const int d = pl.d;
   uint8_t* w = r.w;
@@ -460,8 +467,17 @@ int chunk_forward(Run& r, int64_t r0, int rows, const void* Hc) {
   p.pl = reinterpret_cast<float*>(w + pl.off_pl);
   p.pc = reinterpret_cast<float*>(w + pl.off_pc);
   p.ld_part = pl.rows_alloc;
-  if ((st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_STATS>(KIND_FWD_LOGITS, r.di, p, r.s, "fwd_logits_lse")))
-    return st;
+  if (keep) {
+    if ((st = make_map(&p.tmC, w + pl.off_Z, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, pl.V, rows, uint64_t(pl.ldG) * 4, 32,
+                       32)))
+      return st;
+    p.c_xlim = pl.V;
+    p.c_ylim = rows;
+    st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_KEEP>(KIND_FWD_LOGITS_KEEP, r.di, p, r.s, "fwd_logits_keep");
+  } else {
+    st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_STATS>(KIND_FWD_LOGITS, r.di, p, r.s, "fwd_logits_lse");
+  }
+  if (st) return st;
   const int cblocks = static_cast<int>(cdiv(rows, 32));
   const float* wc = r.weight ? r.weight + r0 : nullptr;
   cudaStream_t s = r.s;
@@ -473,19 +489,15 @@ int chunk_forward(Run& r, int64_t r0, int rows, const void* Hc) {
   });
 }
 
-// Backward of one chunk: recompute the logits into G, then dH_chunk = G W and dW (+)= G^T H_chunk.
-int chunk_backward(Run& r, int64_t r0, int rows, const void* Hc) {
+// G = scale * w_n * (S softmax(z) - p_sparse) of one chunk, from its recomputed logits.
+int grad_recompute(Run& r, int64_t r0, int rows, const void* Hc) {
   const Plan& pl = r.pl;
   const int d = pl.d, V = pl.V;
   uint8_t* w = r.w;
   cudaStream_t s = r.s;
   void* G = w + pl.off_G;
-  float* dhp = reinterpret_cast<float*>(w + pl.off_dhp);
   const int mbr = static_cast<int>(cdiv(rows, TILE_M));
-  const int kb_v = static_cast<int>(cdiv(V, BK));
   int st;
-
-  // --- G = scale * w_n * (S softmax(z) - p_sparse), z recomputed
   TcParams pg;
   memset(&pg, 0, sizeof(pg));
   if ((st = make_map(&pg.tmA, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM))) return st;
@@ -506,8 +518,46 @@ int chunk_backward(Run& r, int64_t r0, int rows, const void* Hc) {
   pg.gscale = r.grad_scale;
   pg.c_xlim = V;
   pg.c_ylim = rows;
-  if ((st = launch_tc<VOCAB_TILE, false, false, EPI_LOGIT_GRAD>(KIND_BWD_GRAD, r.di, pg, s, "bwd_logit_grad")))
-    return st;
+  return launch_tc<VOCAB_TILE, false, false, EPI_LOGIT_GRAD>(KIND_BWD_GRAD, r.di, pg, s, "bwd_logit_grad");
+}
+
+// The same G from the logits the chunk's forward kept (fp32, workspace offset off_Z).
+int grad_from_kept(Run& r, int64_t r0, int rows) {
+  const Plan& pl = r.pl;
+  const int V = pl.V;
+  uint8_t* w = r.w;
+  cudaStream_t s = r.s;
+  const int64_t units = int64_t(rows) * cdiv(V, GRAD_SEG);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(units, int64_t(r.di->sms) * 8)));
+  const float* Z = reinterpret_cast<const float*>(w + pl.off_Z);
+  const int* sidx = reinterpret_cast<const int*>(w + pl.off_sidx);
+  const float* spp = reinterpret_cast<const float*>(w + pl.off_sp);
+  const float* S = reinterpret_cast<const float*>(w + pl.off_S);
+  const float* lse = r.lse + r0;
+  const float* wr = r.weight ? r.weight + r0 : nullptr;
+  const float gsc = r.grad_scale;
+  __nv_bfloat16* Gb = reinterpret_cast<__nv_bfloat16*>(w + pl.off_G);
+  const int K = pl.K, ld = pl.ldG;
+  return launch(KIND_BWD_GRAD_KEPT, s, "bwd_grad_from_logits", [&] {
+    logit_grad_kernel<<<grid, GRAD_THREADS, 0, s>>>(Z, ld, rows, V, K, sidx, spp, S, lse, wr, gsc, Gb);
+  });
+}
+
+// Backward of one chunk: G from recomputed logits (or, with keep, from the logits the chunk's
+// forward stored), then dH_chunk = G W and dW (+)= G^T H_chunk.
+int chunk_backward(Run& r, int64_t r0, int rows, const void* Hc, bool keep = false) {
+  const Plan& pl = r.pl;
+  const int d = pl.d, V = pl.V;
+  uint8_t* w = r.w;
+  cudaStream_t s = r.s;
+  void* G = w + pl.off_G;
+  float* dhp = reinterpret_cast<float*>(w + pl.off_dhp);
+  const int mbr = static_cast<int>(cdiv(rows, TILE_M));
+  const int kb_v = static_cast<int>(cdiv(V, BK));
+  int st;
+
+  // --- G = scale * w_n * (S softmax(z) - p_sparse), z kept or recomputed
+  if ((st = keep ? grad_from_kept(r, r0, rows) : grad_recompute(r, r0, rows, Hc))) return st;
 
   // --- dH_chunk = G W, split over the vocabulary into fp32 partials, then summed
   const int nbd = static_cast<int>(cdiv(d, pl.bn_d));
@@ -642,6 +692,11 @@ size_t fckl_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype
   return make_plan(N, d, V, K, chunk, dtype).total;
 }
 
+size_t fckl_forward_backward_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype) {
+  if (check_shape(N, d, V, K, chunk, dtype) != FCKL_OK) return 0;
+  return make_plan(N, d, V, K, chunk, dtype).total_keep;
+}
+
 int fckl_forward(const void* H, const void* W, int dtype, const int32_t* idx, const float* logp,
                  const float* weight, int64_t N, int d, int V, int K, int chunk, float* loss, float* lse,
                  float* row_loss, void* ws, size_t ws_bytes, void* stream) {
@@ -697,13 +752,14 @@ int fckl_forward_backward(const void* H, const void* W, int dtype, const int32_t
   r.grad_scale = grad_scale;
   r.dH = dH;
   r.dW = dW;
+  const bool keep = ws_bytes >= r.pl.total_keep;
   if ((st = run_begin(r, true))) return st;
   for (int64_t r0 = 0; r0 < N; r0 += r.pl.chunk) {
     const int rows = static_cast<int>(std::min<int64_t>(r.pl.chunk, N - r0));
     const void* Hc = nullptr;
     if ((st = chunk_prepare(r, r0, rows, &Hc))) return st;
-    if ((st = chunk_forward(r, r0, rows, Hc))) return st;
-    if ((st = chunk_backward(r, r0, rows, Hc))) return st;
+    if ((st = chunk_forward(r, r0, rows, Hc, keep))) return st;
+    if ((st = chunk_backward(r, r0, rows, Hc, keep))) return st;
   }
   return run_loss(r, loss);
 }

@@ -288,6 +288,89 @@ __global__ void __launch_bounds__(256) dh_reduce_kernel(const float* __restrict_
   }
 }
 
+// G from the chunk's logits as the forward kept them (fp32 Z, written by the EPI_FWD_KEEP
+// epilogue), instead of recomputing them: G = scale * w_n * (S_n exp(z - lse_n) - p at the
+// cached ids), rounded to bf16, with the same operations in the same order as the
+// EPI_LOGIT_GRAD epilogue, so G is bitwise the one the recomputing path forms.
+// HBM-bound (6 bytes per element): a unit is one position and GRAD_SEG columns; each thread
+// takes 8 adjacent columns per step (two 16-byte streaming loads of Z, one 16-byte store of
+// G), GRAD_STEPS steps 2048 columns apart. The row's ordered cache slots sit in shared memory
+// and each thread walks them with one cursor. Z and G share the row pitch ld (a multiple of
+// 8 elements); columns in [V, ld) of G are written as 0.
+constexpr int GRAD_THREADS = 256;
+constexpr int GRAD_STEPS = 4;
+constexpr int GRAD_SEG = GRAD_THREADS * 8 * GRAD_STEPS;
+
+__global__ void __launch_bounds__(GRAD_THREADS) logit_grad_kernel(
+    const float* __restrict__ Z, int64_t ld, int rows, int V, int K, const int* __restrict__ sidx,
+    const float* __restrict__ sp, const float* __restrict__ S, const float* __restrict__ lse,
+    const float* __restrict__ wrow, float gscale, __nv_bfloat16* __restrict__ G) {
+  __shared__ int s_ids[K_LIMIT];
+  __shared__ float s_p[K_LIMIT];
+  const int segs = (V + GRAD_SEG - 1) / GRAD_SEG;
+  const int64_t units = static_cast<int64_t>(rows) * segs;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int row = static_cast<int>(u / segs);
+    const int seg = static_cast<int>(u - static_cast<int64_t>(row) * segs);
+    __syncthreads();  // every thread is done with the previous unit's slots
+    for (int k = threadIdx.x; k < K; k += GRAD_THREADS) {
+      s_ids[k] = __ldg(sidx + static_cast<int64_t>(row) * K + k);
+      s_p[k] = __ldg(sp + static_cast<int64_t>(row) * K + k);
+    }
+    __syncthreads();
+    const float gs = __fmul_rn(gscale, wrow ? __ldg(wrow + row) : 1.f);
+    const float a = __fmul_rn(gs, __ldg(S + row));
+    const float nl = __fmul_rn(-__ldg(lse + row), LOG2E);
+    const int c0 = seg * GRAD_SEG + 8 * static_cast<int>(threadIdx.x);
+    int lo = 0, hi = K;  // cursor: first slot whose id is >= c0
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_ids[mid] < c0)
+        lo = mid + 1;
+      else
+        hi = mid;
+    }
+    int k = lo;
+    const float* zr = Z + static_cast<int64_t>(row) * ld;
+    __nv_bfloat16* gr = G + static_cast<int64_t>(row) * ld;
+#pragma unroll
+    for (int i = 0; i < GRAD_STEPS; ++i) {
+      const int c = c0 + i * GRAD_THREADS * 8;
+      if (c >= V) break;
+      float x[8];
+      if (c + 8 <= V) {
+        const float4 z0 = __ldcs(reinterpret_cast<const float4*>(zr + c));
+        const float4 z1 = __ldcs(reinterpret_cast<const float4*>(zr + c + 4));
+        x[0] = z0.x, x[1] = z0.y, x[2] = z0.z, x[3] = z0.w;
+        x[4] = z1.x, x[5] = z1.y, x[6] = z1.z, x[7] = z1.w;
+      } else {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) x[t] = c + t < V ? zr[c + t] : 0.f;
+      }
+#pragma unroll
+      for (int t = 0; t < 8; ++t) x[t] = grad_dense(x[t], a, nl);
+      while (k < K && s_ids[k] < c) ++k;
+      while (k < K && s_ids[k] < c + 8) {
+        const int pos = s_ids[k] - c;
+        const float v = __fmul_rn(gs, s_p[k]);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) x[t] = (t == pos) ? __fsub_rn(x[t], v) : x[t];
+        ++k;
+      }
+      if (c + 8 > V) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) x[t] = c + t < V ? x[t] : 0.f;
+      }
+      uint4 w;
+      w.x = pack_bf16x2(x[0], x[1]);
+      w.y = pack_bf16x2(x[2], x[3]);
+      w.z = pack_bf16x2(x[4], x[5]);
+      w.w = pack_bf16x2(x[6], x[7]);
+      *reinterpret_cast<uint4*>(gr + c) = w;
+    }
+  }
+}
+
 // fp32 -> bf16, round to nearest even; n % 4 == 0.
 __global__ void __launch_bounds__(256) cvt_bf16_kernel(const float* __restrict__ src,
                                                        __nv_bfloat16* __restrict__ dst, int64_t n) {

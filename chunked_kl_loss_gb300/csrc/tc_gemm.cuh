@@ -17,6 +17,8 @@
 //                   the gather of the logits at the teacher's cached ids; writes one
 //                   (m, l, c) triple per row and vocabulary tile ("Fused, chunked KL loss":
 //                   fold the chunk's logits into the running loss, then drop them)
+//   EPI_FWD_KEEP  : EPI_FWD_STATS that also stores the fp32 logits tile with TMA, so that
+//                   the chunk's backward can form G from them instead of recomputing them
 //   EPI_LOGIT_GRAD: G = scale * w_n * (S_n exp(z - lse_n) - p at the cached ids), rounded
 //                   to bf16 and stored with TMA (the backward pass recomputes the chunk)
 //   EPI_STORE_F32 : fp32 tile stored, or reduce-added, with TMA (dH partials, dW)
@@ -45,7 +47,7 @@ constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;
 constexpr float LOG2E = 1.4426950408889634f;
 
 enum : unsigned { ST_BAD_INDEX = 1u, ST_TIMEOUT = 2u, ST_CAPACITY = 4u };
-enum { EPI_FWD_STATS = 0, EPI_LOGIT_GRAD = 1, EPI_STORE_F32 = 2, EPI_TOPK_COLLECT = 3 };
+enum { EPI_FWD_STATS = 0, EPI_LOGIT_GRAD = 1, EPI_STORE_F32 = 2, EPI_TOPK_COLLECT = 3, EPI_FWD_KEEP = 4 };
 
 struct Sched {
   int m_blocks, n_blocks, k_blocks;
@@ -180,7 +182,14 @@ __device__ __forceinline__ float pick32(const float (&x)[32], int pos) {
 }
 __device__ __forceinline__ void sub32(float (&x)[32], int pos, float v) {
 #pragma unroll
-  for (int t = 0; t < 32; ++t) x[t] = (t == pos) ? x[t] - v : x[t];
+  for (int t = 0; t < 32; ++t) x[t] = (t == pos) ? __fsub_rn(x[t], v) : x[t];
+}
+
+// One element of G before rounding, with every operation rounded on its own (no contraction
+// into FMAs), so that a kernel forming G from stored logits gets the same bits as the
+// recomputing epilogue: a = scale * w_n * S_n, nl = -lse_n * log2(e).
+__device__ __forceinline__ float grad_dense(float z, float a, float nl) {
+  return __fmul_rn(a, ex2_approx(fmaf(z, LOG2E, nl)));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -414,7 +423,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       const int row0 = mb * BM * CG + static_cast<int>(rank) * BM + 32 * q;  // first row of this warp
       const int row = row0 + lane;
 
-      if constexpr (EPI == EPI_FWD_STATS || EPI == EPI_LOGIT_GRAD) {
+      if constexpr (EPI == EPI_FWD_STATS || EPI == EPI_FWD_KEEP || EPI == EPI_LOGIT_GRAD) {
         const bool valid = row < p.rows_valid;
         const int v0 = nb * BN;
         const int* ids = p.sidx + static_cast<size_t>(valid ? row : 0) * p.K;
@@ -424,17 +433,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           k = lower_bound_ids(ids, p.K, v0);
           nxt = k < p.K ? __ldg(ids + k) : INT_MAX;
         }
-        if constexpr (EPI == EPI_FWD_STATS) {
+        if constexpr (EPI == EPI_FWD_STATS || EPI == EPI_FWD_KEEP) {
           if (!warp_wait_phase(&tfull[acc], use & 1u, abort_flag, p.status)) break;
           tc_fence_after();
           float m = -INFINITY, l = 0.f, c = 0.f;
 #pragma unroll 1
-          for (int j = 0; j < BN / 32; ++j) {
+          for (int j = 0; j < BN / 32; ++j, ++ecnt) {
             float x[32];
             __syncwarp();
             tmem_ld32(taddr + 32 * j, x);
             if (j == BN / 32 - 1) release_acc(acc);
             const int cb = v0 + 32 * j;
+            if constexpr (EPI == EPI_FWD_KEEP) {
+              // stage the raw logits (32 rows x 32 columns, 128-byte swizzle) and store them
+              uint8_t* buf = ebuf0 + (ecnt & 1u) * EPI_BUF_BYTES;
+              if (ecnt >= 2 && lane == 0) bulk_wait_read<1>();
+              __syncwarp();
+#pragma unroll
+              for (int cc = 0; cc < 8; ++cc) {
+                const int chunk16 = cc ^ (lane & 7);
+                *reinterpret_cast<float4*>(buf + lane * 128 + chunk16 * 16) =
+                    make_float4(x[4 * cc + 0], x[4 * cc + 1], x[4 * cc + 2], x[4 * cc + 3]);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                if (cb < p.c_xlim && row0 < p.c_ylim) tma_store_2d(&p.tmC, buf, cb, row0);
+                bulk_commit();
+              }
+            }
             if (cb + 32 > p.V) {
 #pragma unroll
               for (int t = 0; t < 32; ++t)
@@ -463,9 +490,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             p.pc[o] = c;
           }
         } else {
-          const float gs = valid ? p.gscale * (p.wrow ? __ldg(p.wrow + row) : 1.f) : 0.f;
-          const float a = gs * (valid ? __ldg(p.S + row) : 0.f);
-          const float nl = valid ? -__ldg(p.lse + row) * LOG2E : 0.f;
+          const float gs = valid ? __fmul_rn(p.gscale, p.wrow ? __ldg(p.wrow + row) : 1.f) : 0.f;
+          const float a = __fmul_rn(gs, valid ? __ldg(p.S + row) : 0.f);
+          const float nl = valid ? __fmul_rn(-__ldg(p.lse + row), LOG2E) : 0.f;
           if (!warp_wait_phase(&tfull[acc], use & 1u, abort_flag, p.status)) break;
           tc_fence_after();
 #pragma unroll 1
@@ -482,9 +509,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
               if (j == BN / 32 - 1) release_acc(acc);
               const int cb = v0 + 32 * j;
 #pragma unroll
-              for (int t = 0; t < 32; ++t) x[t] = a * ex2_approx(fmaf(x[t], LOG2E, nl));
+              for (int t = 0; t < 32; ++t) x[t] = grad_dense(x[t], a, nl);
               while (nxt < cb + 32) {
-                sub32(x, nxt - cb, gs * __ldg(pr + k));
+                sub32(x, nxt - cb, __fmul_rn(gs, __ldg(pr + k)));
                 ++k;
                 nxt = k < p.K ? __ldg(ids + k) : INT_MAX;
               }

@@ -14,7 +14,9 @@
  *
  * The sequence is walked one chunk of positions at a time: the forward pass projects
  * a chunk, folds it into the running loss and drops it; the backward pass recomputes
- * the chunk's logits to form G. Only a chunk x V gradient slab is ever held.
+ * the chunk's logits to form G (the one-call path may instead keep the chunk's logits from
+ * its forward, see fckl_forward_backward_workspace_bytes). Only one chunk's slabs (G, and
+ * the kept logits) are ever held.
  *
  * Conventions for every call below
  *  - All arrays are dense and row-major. "device" pointers are CUDA device memory of the
@@ -73,6 +75,14 @@ typedef enum { FCKL_BF16 = 0, FCKL_F32 = 1 } fckl_dtype;
  * position; 0 if the shape is outside the limits. */
 size_t fckl_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
 
+/* Workspace with which fckl_forward_backward keeps each chunk's logits between its forward
+ * and its backward: fckl_workspace_bytes() plus one chunk of fp32 logits (chunk x V, rows
+ * padded to 256 and to a multiple of 8 columns). Not an operation of the pages' method but
+ * a trade of memory for compute that the one-call path allows: the logits of a chunk are
+ * recomputed in the backward there only because the forward drops them ("Fused, chunked KL
+ * loss"); here one chunk's worth is held, still independent of N. 0 outside the limits. */
+size_t fckl_forward_backward_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
+
 /* Forward pass.
  *   loss     : device fp32 [1]  <- sum over positions of the per-position KL (a SUM, not a mean)
  *   lse      : device fp32 [N]  <- log-partition of every position, kept for fckl_backward
@@ -99,7 +109,12 @@ int fckl_backward(const void* H, const void* W, int dtype,
 /* Forward and backward in one call, chunk by chunk: each chunk's backward runs right after
  * its forward (lse_n depends on position n alone), so the chunk's cache slots are ordered
  * once and its hidden states are re-read while still in L2. Outputs as fckl_forward and
- * fckl_backward (row_loss may be NULL); same workspace size. */
+ * fckl_backward (row_loss may be NULL).
+ * Workspace: at least fckl_workspace_bytes(); with ws_bytes >=
+ * fckl_forward_backward_workspace_bytes() the forward also stores each chunk's fp32 logits
+ * and the backward forms G from them instead of recomputing the logits (one product of the
+ * four per chunk saved, for 4 * chunk * V more bytes of workspace). Both ways compute the
+ * same operations on the same values: the outputs are bitwise identical. */
 int fckl_forward_backward(const void* H, const void* W, int dtype,
                           const int32_t* idx, const float* logp, const float* weight,
                           int64_t N, int d, int V, int K, int chunk, float grad_scale,
