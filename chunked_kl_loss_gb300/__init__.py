@@ -68,6 +68,8 @@ def load():
     lib.fckl_selftest_wait_timeout.argtypes = [vp, sz, vp]
     lib.fckl_topk_workspace_bytes.restype = sz
     lib.fckl_topk_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
+    lib.fckl_topk_kept_logits_workspace_bytes.restype = sz
+    lib.fckl_topk_kept_logits_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
     lib.fckl_teacher_topk.restype = i32
     lib.fckl_teacher_topk.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, vp, vp, vp, sz, vp]
     lib.fckl_check.restype = i32
@@ -117,12 +119,15 @@ def forward_backward_workspace_bytes(N: int, d: int, V: int, K: int, chunk: int,
 
 class Workspace:
     """A device workspace sized for one problem shape (a torch uint8 tensor); ``kind`` is
-    "loss" (forward/backward), "fused" (forward_backward keeping each chunk's logits) or
-    "topk" (teacher cache builder)."""
+    "loss" (forward/backward), "fused" (forward_backward keeping each chunk's logits),
+    "topk" (teacher cache builder keeping each chunk's logits) or "topk_min" (the builder's
+    minimum, which projects each chunk twice)."""
 
     def __init__(self, N, d, V, K, chunk, dtype=BF16, device=None, kind="loss"):
         import torch
         if kind == "topk":
+            n = int(load().fckl_topk_kept_logits_workspace_bytes(N, d, V, K, chunk, dtype))
+        elif kind == "topk_min":
             n = int(load().fckl_topk_workspace_bytes(N, d, V, K, chunk, dtype))
         elif kind == "fused":
             n = forward_backward_workspace_bytes(N, d, V, K, chunk, dtype)
@@ -284,9 +289,11 @@ def fused_chunked_kl(H, W, idx, logp, chunk, weight=None):
     return _FusedChunkedKL.apply(H, W, idx, logp, chunk, weight)
 
 
-def teacher_topk(Ht, Wt, K, chunk, ws=None, stream=None):
+def teacher_topk(Ht, Wt, K, chunk, ws=None, stream=None, keep_logits=True):
     """Offline teacher cache: (idx int32 [N, K], logp fp32 [N, K]) — the K tokens of largest
-    teacher logit per position, by logit descending, with full-softmax log-probabilities."""
+    teacher logit per position, by logit descending, with full-softmax log-probabilities.
+    ``keep_logits=False`` hands the library only the minimum workspace, so it projects each
+    chunk twice instead of keeping its logits; the outputs are the same."""
     import torch
     N, d = Ht.shape
     V = Wt.shape[0]
@@ -299,14 +306,16 @@ def teacher_topk(Ht, Wt, K, chunk, ws=None, stream=None):
     global _last_ws
     import weakref
     if ws is None:
-        ws = Workspace(N, d, V, K, chunk, dt, Ht.device, kind="topk")
+        ws = Workspace(N, d, V, K, chunk, dt, Ht.device, kind="topk" if keep_logits else "topk_min")
         _last_ws = ws
     else:
         _last_ws = weakref.ref(ws)
+    nbytes = ws.nbytes if keep_logits else min(ws.nbytes, int(load().fckl_topk_workspace_bytes(N, d, V, K, chunk,
+                                                                                                 dt)))
     idx = torch.empty(N, K, dtype=torch.int32, device=Ht.device)
     logp = torch.empty(N, K, dtype=torch.float32, device=Ht.device)
     st = load().fckl_teacher_topk(_ptr(Ht), _ptr(Wt), dt, N, d, V, K, chunk, _ptr(idx), _ptr(logp), ws.ptr,
-                                  ws.nbytes, _stream_ptr(stream))
+                                  nbytes, _stream_ptr(stream))
     if st != OK:
         raise FcklError(st, "fckl_teacher_topk")
     return idx, logp

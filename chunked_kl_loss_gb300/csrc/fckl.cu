@@ -46,6 +46,8 @@ enum Kind {
   KIND_TOPK_SELECT,
   KIND_FWD_LOGITS_KEEP,
   KIND_BWD_GRAD_KEPT,
+  KIND_TOPK_LOGITS_KEEP,
+  KIND_TOPK_COLLECT_KEPT,
   KIND_COUNT
 };
 const char* const kKindNames[KIND_COUNT] = {"preprocess",     "fwd_logits_lse", "fwd_combine",
@@ -53,7 +55,8 @@ const char* const kKindNames[KIND_COUNT] = {"preprocess",     "fwd_logits_lse", 
                                             "bwd_dH_reduce",  "bwd_dW_gemm",    "cvt_bf16",
                                             "wait_timeout_selftest", "topk_logits_stats", "topk_threshold",
                                             "topk_collect",           "topk_select",
-                                            "fwd_logits_keep",        "bwd_grad_from_logits"};
+                                            "fwd_logits_keep",        "bwd_grad_from_logits",
+                                            "topk_logits_keep",       "topk_collect_from_logits"};
 
 // ------------------------------------------------------------------ process state
 std::mutex g_mu;
@@ -646,7 +649,9 @@ constexpr size_t TOPK_THR_SMEM = 160 * 1024;  // shared-memory budget of the thr
 struct TopkPlan {
   int chunk, rows_alloc, tiles_v, cmax;
   int thr_rows, thr_stride;  // threshold kernel: positions per block, shared-memory row pitch
+  int ldz;  // row pitch (elements) of the kept logits
   size_t off_status, off_pm, off_pl, off_pc, off_lse, off_thr, off_cnt, off_cv, off_cz, off_Hb, off_Wb, total;
+  size_t off_Z, total_keep;  // the chunk's fp32 logits from pass 1, read by the collect step
 };
 
 TopkPlan make_topk_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
@@ -677,6 +682,9 @@ TopkPlan make_topk_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
   p.off_Hb = dt == FCKL_F32 ? take(R * d * 2) : o;
   p.off_Wb = dt == FCKL_F32 ? take(static_cast<size_t>(V) * d * 2) : o;
   p.total = o;
+  p.ldz = static_cast<int>(rup(V, 8));
+  p.off_Z = take(R * p.ldz * 4);
+  p.total_keep = o;
   return p;
 }
 
@@ -785,6 +793,11 @@ size_t fckl_topk_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int 
   return make_topk_plan(N, d, V, K, chunk, dtype).total;
 }
 
+size_t fckl_topk_kept_logits_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype) {
+  if (check_shape(N, d, V, K, chunk, dtype) != FCKL_OK) return 0;
+  return make_topk_plan(N, d, V, K, chunk, dtype).total_keep;
+}
+
 int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int d, int V, int K, int chunk,
                       int32_t* idx, float* logp, void* ws, size_t ws_bytes, void* stream) {
   int st = check_shape(N, d, V, K, chunk, dtype);
@@ -795,6 +808,7 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
   const TopkPlan tp = make_topk_plan(N, d, V, K, chunk, dtype);
   if (static_cast<size_t>(tp.thr_rows) * tp.thr_stride * 4 > TOPK_THR_SMEM) return FCKL_ERR_UNSUPPORTED;
   if (ws_bytes < tp.total) return FCKL_ERR_WORKSPACE;
+  const bool keep = ws_bytes >= tp.total_keep;
   DevInfo* di = nullptr;
   if ((st = device_info(&di))) return st;
   {
@@ -857,8 +871,17 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
     p.pl = pl;
     p.pc = reinterpret_cast<float*>(w + tp.off_pc);
     p.ld_part = tp.rows_alloc;
-    if ((st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_STATS>(KIND_TOPK_LOGITS, di, p, s, "topk_logits_stats")))
-      return st;
+    float* Z = reinterpret_cast<float*>(w + tp.off_Z);
+    if (keep) {  // pass 1 also stores the logits for the collect step
+      if ((st = make_map(&p.tmC, Z, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, V, rows, uint64_t(tp.ldz) * 4, 32, 32)))
+        return st;
+      p.c_xlim = V;
+      p.c_ylim = rows;
+      st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_KEEP>(KIND_TOPK_LOGITS_KEEP, di, p, s, "topk_logits_keep");
+    } else {
+      st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_STATS>(KIND_TOPK_LOGITS, di, p, s, "topk_logits_stats");
+    }
+    if (st) return st;
     const int wblocks = static_cast<int>(cdiv(rows, 4));
     const int ld = tp.rows_alloc, tiles = tp.tiles_v;
     const int tR = tp.thr_rows, tstride = tp.thr_stride;
@@ -869,17 +892,27 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
                                                              cnt);
          })))
       return st;
-    // pass 2: the logits recomputed; every logit at or above the threshold becomes a candidate
-    p.thr = thr;
-    p.cnt = cnt;
-    p.cand_v = cv;
-    p.cand_z = cz;
-    p.cmax = tp.cmax;
-    if ((st = launch_tc<VOCAB_TILE, false, false, EPI_TOPK_COLLECT>(KIND_TOPK_COLLECT, di, p, s, "topk_collect")))
-      return st;
+    // pass 2: every logit at or above the threshold becomes a candidate (logits kept from
+    // pass 1, or recomputed)
+    const int cmax = tp.cmax;
+    if (keep) {
+      const int64_t units = int64_t(rows) * cdiv(V, GRAD_SEG);
+      const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(units, int64_t(di->sms) * 8)));
+      const int64_t ldz = tp.ldz;
+      st = launch(KIND_TOPK_COLLECT_KEPT, s, "topk_collect_from_logits", [&] {
+        topk_collect_kernel<<<grid, GRAD_THREADS, 0, s>>>(Z, ldz, rows, V, thr, cnt, cv, cz, cmax);
+      });
+    } else {
+      p.thr = thr;
+      p.cnt = cnt;
+      p.cand_v = cv;
+      p.cand_z = cz;
+      p.cmax = cmax;
+      st = launch_tc<VOCAB_TILE, false, false, EPI_TOPK_COLLECT>(KIND_TOPK_COLLECT, di, p, s, "topk_collect");
+    }
+    if (st) return st;
     int32_t* io = idx + r0 * K;
     float* lo = logp + r0 * K;
-    const int cmax = tp.cmax;
     if ((st = launch(KIND_TOPK_SELECT, s, "topk_select", [&] {
            topk_select_kernel<<<wblocks, 128, 0, s>>>(cv, cz, cnt, cmax, rows, K, lse, io, lo, status);
          })))

@@ -12,6 +12,11 @@ namespace fckl {
 
 constexpr int PRE_WARPS = 4;
 constexpr int K_LIMIT = 1024;
+// Kernels that stream a chunk's kept fp32 logits: threads per block, steps of 8 columns per
+// thread, and the columns of one unit (one position).
+constexpr int GRAD_THREADS = 256;
+constexpr int GRAD_STEPS = 4;
+constexpr int GRAD_SEG = GRAD_THREADS * 8 * GRAD_STEPS;
 
 // One warp per position of the chunk. Validates the teacher ids, orders the K slots by
 // (id, slot) so the epilogues can walk them with a cursor, and forms p = exp(logp),
@@ -205,6 +210,64 @@ __global__ void __launch_bounds__(256) topk_threshold_kernel(const float* __rest
   }
 }
 
+// Teacher cache builder, candidate collection from the logits pass 1 kept (fp32 Z, row pitch
+// ld): every logit at or above the position's threshold is appended, with its token id, to
+// the position's candidate list. The same values are compared with the same threshold as in
+// the recomputing collect epilogue, so the candidate set is the same (the append order is
+// not fixed in either; the select step orders the candidates fully). HBM-bound (4 bytes per
+// element); units of one position and GRAD_SEG columns, 8 adjacent columns per thread and
+// step, as in logit_grad_kernel.
+__global__ void __launch_bounds__(GRAD_THREADS) topk_collect_kernel(
+    const float* __restrict__ Z, int64_t ld, int rows, int V, const float* __restrict__ thr,
+    int* __restrict__ cnt, int* __restrict__ cand_v, float* __restrict__ cand_z, int cmax) {
+  const int segs = (V + GRAD_SEG - 1) / GRAD_SEG;
+  const int64_t units = static_cast<int64_t>(rows) * segs;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int row = static_cast<int>(u / segs);
+    const int seg = static_cast<int>(u - static_cast<int64_t>(row) * segs);
+    const float* zr = Z + static_cast<int64_t>(row) * ld;
+    const int c0 = seg * GRAD_SEG + 8 * static_cast<int>(threadIdx.x);
+    // all loads of the unit first (up to 2 * GRAD_STEPS 16-byte loads in flight per thread)
+    float4 z[2 * GRAD_STEPS];
+#pragma unroll
+    for (int i = 0; i < GRAD_STEPS; ++i) {
+      const int c = c0 + i * GRAD_THREADS * 8;
+      if (c + 8 <= V) {
+        z[2 * i] = __ldcs(reinterpret_cast<const float4*>(zr + c));
+        z[2 * i + 1] = __ldcs(reinterpret_cast<const float4*>(zr + c + 4));
+      } else {
+        float x[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) x[t] = c + t < V ? zr[c + t] : -INFINITY;
+        z[2 * i] = make_float4(x[0], x[1], x[2], x[3]);
+        z[2 * i + 1] = make_float4(x[4], x[5], x[6], x[7]);
+      }
+    }
+    const float th = __ldg(thr + row);
+#pragma unroll
+    for (int i = 0; i < GRAD_STEPS; ++i) {
+      const int c = c0 + i * GRAD_THREADS * 8;
+      const float x[8] = {z[2 * i].x, z[2 * i].y, z[2 * i].z, z[2 * i].w,
+                          z[2 * i + 1].x, z[2 * i + 1].y, z[2 * i + 1].z, z[2 * i + 1].w};
+      uint32_t hits = 0;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) hits |= (x[t] >= th && c + t < V) ? (1u << t) : 0u;
+      while (hits) {
+        const int t = __ffs(hits) - 1;
+        hits &= hits - 1;
+        const int pos = atomicAdd(cnt + row, 1);
+        if (pos < cmax) {
+          float v = x[0];
+#pragma unroll
+          for (int q = 1; q < 8; ++q) v = (q == t) ? x[q] : v;
+          cand_v[static_cast<int64_t>(row) * cmax + pos] = c + t;
+          cand_z[static_cast<int64_t>(row) * cmax + pos] = v;
+        }
+      }
+    }
+  }
+}
+
 // Teacher cache builder, last step. One warp per position: ranks the row's candidates by
 // (logit descending, token id ascending) and writes the first K as (id, logit - lse).
 // A row with more candidates than the buffer holds raises ST_CAPACITY (its output is then
@@ -297,9 +360,6 @@ __global__ void __launch_bounds__(256) dh_reduce_kernel(const float* __restrict_
 // G), GRAD_STEPS steps 2048 columns apart. The row's ordered cache slots sit in shared memory
 // and each thread walks them with one cursor. Z and G share the row pitch ld (a multiple of
 // 8 elements); columns in [V, ld) of G are written as 0.
-constexpr int GRAD_THREADS = 256;
-constexpr int GRAD_STEPS = 4;
-constexpr int GRAD_SEG = GRAD_THREADS * 8 * GRAD_STEPS;
 
 __global__ void __launch_bounds__(GRAD_THREADS) logit_grad_kernel(
     const float* __restrict__ Z, int64_t ld, int rows, int V, int K, const int* __restrict__ sidx,

@@ -164,14 +164,17 @@ int fckl_forward_static(const void* H, const void* W, int dtype,
  * z_nv = Wt_v . h_n and their log-probabilities under the full softmax, z_nv - lse_n:
  *   idx  : device int32 [N, K], each row ordered by logit descending, equal logits by smaller id
  *   logp : device fp32  [N, K]
- * The logits are projected twice per chunk and never stored: the first pass keeps each row's
- * per-tile maxima and sum-exp (giving lse_n and a threshold, the K-th largest tile maximum,
- * that every top-K logit reaches); the second keeps the logits at or above the threshold as
- * candidates, which are then ranked exactly. A row with more candidates than the buffer holds
- * (min(V, 2048) slots, or V when K exceeds ceil(V/256)) is reported as FCKL_ERR_CAPACITY by
- * fckl_check. The workspace is sized by fckl_topk_workspace_bytes. V up to 1,310,720
- * (FCKL_ERR_UNSUPPORTED above). */
+ * Two passes per chunk: the first projects the chunk and keeps each row's per-tile maxima and
+ * sum-exp (giving lse_n and a threshold, the K-th largest tile maximum, that every top-K
+ * logit reaches); the second keeps the logits at or above the threshold as candidates, which
+ * are then ranked exactly. The second pass reads the chunk's logits as the first pass stored
+ * them when ws_bytes >= fckl_topk_kept_logits_workspace_bytes() (4 * chunk * V bytes more),
+ * else it projects the chunk again; the outputs are the same either way. A row with more
+ * candidates than the buffer holds (min(V, 2048) slots, or V when K exceeds ceil(V/256)) is
+ * reported as FCKL_ERR_CAPACITY by fckl_check. The workspace is at least
+ * fckl_topk_workspace_bytes. V up to 1,310,720 (FCKL_ERR_UNSUPPORTED above). */
 size_t fckl_topk_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
+size_t fckl_topk_kept_logits_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
 int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype,
                       int64_t N, int d, int V, int K, int chunk,
                       int32_t* idx, float* logp,

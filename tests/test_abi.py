@@ -63,6 +63,13 @@ def test_workspace_size_rules(fckl):
         rows = -(-min(chunk, N) // 256) * 256
         assert 0 <= extra - rows * (-(-V // 8) * 8) * 4 < 1024
     assert fb(64, 250, 4096, 16, 16, fckl.BF16) == 0
+    # the top-K builder's kept logits: the same slab on top of its minimum workspace
+    lib = fckl.load()
+    for N, d, V, K, chunk in [(32768, 3072, 128256, 100, 2048), (130, 320, 2057, 100, 200)]:
+        extra = (lib.fckl_topk_kept_logits_workspace_bytes(N, d, V, K, chunk, fckl.BF16)
+                 - lib.fckl_topk_workspace_bytes(N, d, V, K, chunk, fckl.BF16))
+        rows = -(-min(chunk, N) // 256) * 256
+        assert 0 <= extra - rows * (-(-V // 8) * 8) * 4 < 1024
     # outside the limits: 0
     assert ws(0, 256, 4096, 16, 16, fckl.BF16) == 0
     assert ws(64, 250, 4096, 16, 16, fckl.BF16) == 0  # d % 8 != 0

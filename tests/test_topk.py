@@ -113,3 +113,38 @@ def test_topk_is_deterministic(fckl):
     b = run_topk(fckl, Ht, Wt, 50, 100)
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("N,d,V,K,chunk", [
+    (300, 256, 5000, 40, 128),
+    (64, 128, 1000, 20, 64),      # every token a candidate
+    (130, 320, 2057, 100, 200),   # V % 8 == 1: a partial group of 8 columns per position
+])
+def test_topk_kept_and_recomputed_logits_agree(fckl, N, d, V, K, chunk):
+    """Pass 2 reading the logits pass 1 kept gives the cache that projecting again gives, bit
+    for bit; the profile counters show which kernels ran."""
+    rng = np.random.default_rng(N + V + K)
+    Ht = synthetic.round_bf16(rng.standard_normal((N, d), dtype=np.float32))
+    Wt = synthetic.round_bf16(rng.standard_normal((V, d), dtype=np.float32) * 3.0 / np.sqrt(d))
+    dev = torch.device("cuda")
+    H = torch.from_numpy(Ht).to(dev).to(torch.bfloat16)
+    W = torch.from_numpy(Wt).to(dev).to(torch.bfloat16)
+    out = {}
+    for keep in (True, False):
+        fckl.profile_enable(True)
+        fckl.profile_read()
+        out[keep] = fckl.teacher_topk(H, W, K, chunk, keep_logits=keep)
+        prof = fckl.profile_read()
+        fckl.profile_enable(False)
+        assert fckl.check() == fckl.OK
+        ran = {k for k, (_, n) in prof.items() if n > 0}
+        if keep:
+            assert {"topk_logits_keep", "topk_collect_from_logits"} <= ran
+            assert not ran & {"topk_logits_stats", "topk_collect"}
+        else:
+            assert {"topk_logits_stats", "topk_collect"} <= ran
+            assert not ran & {"topk_logits_keep", "topk_collect_from_logits"}
+    assert torch.equal(out[True][0], out[False][0])
+    assert torch.equal(out[True][1], out[False][1])
+    idx, logp = (t.cpu().numpy() for t in out[True])
+    assert_topk_parity(idx.astype(np.int64), logp.astype(np.float64), Ht, Wt, K)
