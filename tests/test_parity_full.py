@@ -1,10 +1,13 @@
-"""GPU parity at the full workload sizes, in the launch configuration bench.py times.
+"""GPU parity at the full workload sizes, in the launch configuration bench.py times (one
+fckl_forward_backward call with a "fused" workspace: each chunk's logits kept from its
+forward for its backward).
 
 At these sizes the oracle cannot run the whole problem in a test, so it checks what it can
 compute one position at a time — lse_n, the per-position loss and the dH row of sampled
 positions, each depending only on its own logits row — and the rest through properties that
 hold at any size: the vocabulary sum of dW vanishes (the rows of G sum to zero) and the
-reported loss is the sum of the per-position losses.
+reported loss is the sum of the per-position losses. At the headline size the separate
+forward and backward calls (logits recomputed) must give the same bits.
 """
 import numpy as np
 import pytest
@@ -28,13 +31,17 @@ def test_full_size_sampled_rows_and_properties(fckl, name):
     W = torch.from_numpy(x["W"]).to(dev).to(torch.bfloat16)
     idx = torch.from_numpy(x["idx"]).to(dev)
     logp = torch.from_numpy(x["logp"]).to(dev)
-    # the oracle sees exactly the bf16 values the device sees
-    Hq = H[:0]
-    ws = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, fckl.BF16)
-    loss, lse, rl = fckl.forward(H, W, idx, logp, w.chunk, ws=ws, row_loss=True)
-    fckl.check(ws)
-    dH, dW = fckl.backward(H, W, idx, logp, lse, w.chunk, grad_scale=1.0, ws=ws)
-    fckl.check(ws)
+    ws = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, fckl.BF16, kind="fused")
+    loss, lse, rl, dH, dW = fckl.forward_backward(H, W, idx, logp, w.chunk, ws=ws, row_loss=True)
+    assert fckl.check(ws) == fckl.OK
+    if name == "n32768_d3072_v128256":
+        ws2 = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, fckl.BF16)
+        loss2, lse2, rl2 = fckl.forward(H, W, idx, logp, w.chunk, ws=ws2, row_loss=True)
+        dH2, dW2 = fckl.backward(H, W, idx, logp, lse2, w.chunk, ws=ws2)
+        assert fckl.check(ws2) == fckl.OK
+        for a, b in ((loss, loss2), (lse, lse2), (rl, rl2), (dH, dH2), (dW, dW2)):
+            assert torch.equal(a, b)
+        del ws2, loss2, lse2, rl2, dH2, dW2
 
     rng = np.random.default_rng(123)
     rows = np.unique(np.concatenate([[0, w.chunk - 1, w.chunk, w.N - 1], rng.integers(0, w.N, 4)]))
@@ -61,4 +68,3 @@ def test_full_size_sampled_rows_and_properties(fckl, name):
     p2 = torch.from_numpy((np.exp(x["logp"].astype(np.float64)) ** 2).sum(1)).to(dev)
     sig = (2.0 ** -8 / np.sqrt(3.0)) * torch.sqrt((H.double() ** 2 * p2[:, None]).sum(0)).cpu().numpy()
     assert np.all(np.abs(col) <= 6.0 * sig + 1e-4 * dW.abs().max().item()), (np.abs(col) / sig).max()
-    del Hq
