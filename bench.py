@@ -337,33 +337,60 @@ def run_ours(args):
 
     t_max = max_over_ranks(elapsed_ms, dev)
 
-    # end to end through the public API from pinned host buffers
+    # end to end through the public API from pinned host buffers: every step copies its inputs
+    # from pinned host memory and reads its loss back. The copies of step i+1 run on a second
+    # stream into the other of two device input sets while step i computes, as a training
+    # loop that prefetches its next batch would; all of them fall inside the timed region.
     e2e = None
     if not args.no_e2e:
-        loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+        loss_host = torch.empty(args.steps + 1, dtype=torch.float32).pin_memory()
+        bufs = [{k: torch.empty_like(host[k], device=dev) for k in host} for _ in range(2)]
+        copy_stream = torch.cuda.Stream(dev)
+        copied = [torch.cuda.Event() for _ in range(2)]
+        freed = [torch.cuda.Event() for _ in range(2)]
 
-        def e2e_step():
-            Hd, Wd, idd, lpd = (host[k].to(dev, non_blocking=True) for k in ("H", "W", "idx", "logp"))
-            if args.api == "fused":
-                loss, _, _, _ = fckl.forward_backward(Hd, Wd, idd, lpd, w.chunk, ws=ws, stream=stream, dH=dH,
-                                                      dW=dW, keep_logits=keep)
-            else:
-                loss, lse = fckl.forward(Hd, Wd, idd, lpd, w.chunk, ws=ws, stream=stream)
-                fckl.backward(Hd, Wd, idd, lpd, lse, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW)
-            loss_host.copy_(loss, non_blocking=True)
+        def issue_copy(i):
+            j = i % 2
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(freed[j])  # step i-2, the last reader of set j, is done
+                for k in host:
+                    bufs[j][k].copy_(host[k], non_blocking=True)
+                copied[j].record(copy_stream)
 
-        e2e_step()
+        def e2e_run(n):
+            for j in range(2):
+                freed[j].record(stream)
+            issue_copy(0)
+            for i in range(n):
+                if i + 1 < n:
+                    issue_copy(i + 1)
+                j = i % 2
+                stream.wait_event(copied[j])
+                b = bufs[j]
+                if args.api == "fused":
+                    loss, _, _, _ = fckl.forward_backward(b["H"], b["W"], b["idx"], b["logp"], w.chunk, ws=ws,
+                                                          stream=stream, dH=dH, dW=dW, keep_logits=keep)
+                else:
+                    loss, lse = fckl.forward(b["H"], b["W"], b["idx"], b["logp"], w.chunk, ws=ws, stream=stream)
+                    fckl.backward(b["H"], b["W"], b["idx"], b["logp"], lse, w.chunk, ws=ws, stream=stream, dH=dH,
+                                  dW=dW)
+                freed[j].record(stream)
+                loss_host[i:i + 1].copy_(loss, non_blocking=True)
+
+        e2e_run(2)
         barrier()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        copy_stream.wait_event(f0)  # the first copy starts inside the timed region
+        e2e_run(args.steps)
         f1.record(stream)
         barrier()
         e2e_ms = max_over_ranks(f0.elapsed_time(f1), dev)
         h2d = sum(host[k].numel() * host[k].element_size() for k in host)
         e2e = {"value": world * w.N * args.steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": 4, "ms_per_step": e2e_ms / args.steps}
+               "d2h_bytes_per_step": 4, "ms_per_step": e2e_ms / args.steps,
+               "copies": "step i+1's inputs copied on a second stream while step i computes (two device input "
+                         "sets); every step's copies and loss read-back inside the timed region"}
 
     if rank != 0:
         if world > 1:
