@@ -3,9 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 One step = one forward + backward over the whole workload (all chunks), inputs resident in
-HBM: one fckl_forward_backward call (--api fused, the default; each chunk's logits kept from
-its forward for its backward, or recomputed with --recompute) or fckl_forward then
-fckl_backward (--api separate, which recomputes). Prints one JSON line (rank 0). Under torchrun each rank runs its own
+HBM: one fckl_forward_backward call (--api fused, the default: each chunk's backward forms G
+from what its forward kept in the gradient slab) or fckl_forward then fckl_backward (--api
+separate: the backward recomputes each chunk's logits). Prints one JSON line (rank 0). Under torchrun each rank runs its own
 replica of the workload (the loss has no exchange step on one GPU: replicas only) and
 the whole-job value is the positions of all ranks over the slowest rank's time.
 
@@ -57,9 +57,7 @@ def parse():
     ap.add_argument("--api", default="fused", choices=["fused", "separate"],
                     help="one fckl_forward_backward call per step, or fckl_forward then fckl_backward")
     ap.add_argument("--recompute", action="store_true",
-                    help="--api fused: recompute each chunk's logits in its backward instead of keeping "
-                         "them from its forward; --topk: project each chunk twice instead of keeping its "
-                         "logits from pass 1")
+                    help="--topk: project each chunk twice instead of keeping its logits from pass 1")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -129,7 +127,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": config_of(w, args.api, args.recompute),
+            "config": config_of(w, args.api),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
                              "sample": f"each step: fp64 oracle forward+backward on {n} of {w.N} positions "
                                        f"(full V, d)"},
@@ -138,14 +136,11 @@ def run_reference(args):
     return 0
 
 
-def logits_kept(api, recompute):
-    return api == "fused" and not recompute
-
-
-def config_of(w, api="fused", recompute=False):
+def config_of(w, api="fused"):
     return {"workload": w.name, "N": w.N, "d": w.d, "V": w.V, "K": w.K, "chunk": w.chunk,
             "input_dtype": w.dtype, "parallelism": "replicas", "api": api,
-            "logits": "kept from the forward" if logits_kept(api, recompute) else "recomputed in the backward",
+            "logits": ("kept by the forward (fp16 exp(z - tile max) in the gradient slab)" if api == "fused"
+                       else "recomputed in the backward"),
             "l2": "inputs larger than L2 (W alone is %.0f MB)" % (w.V * w.d * 2 / 1e6)}
 
 
@@ -289,16 +284,15 @@ def run_ours(args):
     base_alloc = torch.cuda.memory_allocated(dev)
     H, W, idx, logp = (host[k].to(dev) for k in ("H", "W", "idx", "logp"))
     dt = fckl.BF16 if w.dtype == "bf16" else fckl.F32
-    keep = logits_kept(args.api, args.recompute)
-    ws = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, dt, dev, kind="fused" if keep else "loss")
+    keep = args.api == "fused"
+    ws = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, dt, dev)
     dH = torch.empty_like(H)
     dW = torch.empty(w.V, w.d, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         if args.api == "fused":
-            loss, _, _, _ = fckl.forward_backward(H, W, idx, logp, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW,
-                                                  keep_logits=keep)
+            loss, _, _, _ = fckl.forward_backward(H, W, idx, logp, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW)
             return loss
         loss, lse = fckl.forward(H, W, idx, logp, w.chunk, ws=ws, stream=stream)
         fckl.backward(H, W, idx, logp, lse, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW)
@@ -369,7 +363,7 @@ def run_ours(args):
                 b = bufs[j]
                 if args.api == "fused":
                     loss, _, _, _ = fckl.forward_backward(b["H"], b["W"], b["idx"], b["logp"], w.chunk, ws=ws,
-                                                          stream=stream, dH=dH, dW=dW, keep_logits=keep)
+                                                          stream=stream, dH=dH, dW=dW)
                 else:
                     loss, lse = fckl.forward(b["H"], b["W"], b["idx"], b["logp"], w.chunk, ws=ws, stream=stream)
                     fckl.backward(b["H"], b["W"], b["idx"], b["logp"], lse, w.chunk, ws=ws, stream=stream, dH=dH,
@@ -423,7 +417,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generators; no dataset)",
-        "config": config_of(w, args.api, args.recompute),
+        "config": config_of(w, args.api),
         "tflops": tflops, "tflops_executed": tflops_exec, "tflops_executed_frac_of_peak": tflops_exec / peak_sus,
         "peak_gib": peak_bytes / 2**30,
         "gpu_launches": launches,
@@ -469,7 +463,7 @@ def memory_sweep(args):
         torch.cuda.reset_peak_memory_stats(dev)
         H = Hh[:n].to(dev)
         idx, logp = idx_h[:n].to(dev), logp_h[:n].to(dev)
-        ws = fckl.Workspace(n, w.d, w.V, w.K, w.chunk, fckl.BF16, dev, kind="fused" if fused else "loss")
+        ws = fckl.Workspace(n, w.d, w.V, w.K, w.chunk, fckl.BF16, dev)
         if fused:
             fckl.forward_backward(H, W, idx, logp, w.chunk, ws=ws)
         else:
@@ -491,7 +485,7 @@ def memory_sweep(args):
     fused = fit([(n, peak_of(n, True)) for n in sizes])
     line = {"metric": "peak device memory of one forward+backward vs N (GiB)", "workload": w.name,
             "chunk": w.chunk, "analytic_bytes_per_position": bytes_per_position(w),
-            "separate_calls_logits_recomputed": sep, "one_call_logits_kept": fused}
+            "separate_calls": sep, "one_call": fused}
     print(json.dumps(line), flush=True)
     return line
 

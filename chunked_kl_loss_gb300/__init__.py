@@ -55,8 +55,6 @@ def load():
     vp, i64, i32, sz, f32 = c.c_void_p, c.c_int64, c.c_int, c.c_size_t, c.c_float
     lib.fckl_workspace_bytes.restype = sz
     lib.fckl_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
-    lib.fckl_forward_backward_workspace_bytes.restype = sz
-    lib.fckl_forward_backward_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
     lib.fckl_forward.restype = i32
     lib.fckl_forward.argtypes = [vp, vp, i32, vp, vp, vp, i64, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
     lib.fckl_backward.restype = i32
@@ -113,15 +111,10 @@ def workspace_bytes(N: int, d: int, V: int, K: int, chunk: int, dtype: int = BF1
     return int(load().fckl_workspace_bytes(N, d, V, K, chunk, dtype))
 
 
-def forward_backward_workspace_bytes(N: int, d: int, V: int, K: int, chunk: int, dtype: int = BF16) -> int:
-    return int(load().fckl_forward_backward_workspace_bytes(N, d, V, K, chunk, dtype))
-
-
 class Workspace:
     """A device workspace sized for one problem shape (a torch uint8 tensor); ``kind`` is
-    "loss" (forward/backward), "fused" (forward_backward keeping each chunk's logits),
-    "topk" (teacher cache builder keeping each chunk's logits) or "topk_min" (the builder's
-    minimum, which projects each chunk twice)."""
+    "loss" (forward, backward, forward_backward), "topk" (teacher cache builder keeping each
+    chunk's logits) or "topk_min" (the builder's minimum, which projects each chunk twice)."""
 
     def __init__(self, N, d, V, K, chunk, dtype=BF16, device=None, kind="loss"):
         import torch
@@ -129,8 +122,6 @@ class Workspace:
             n = int(load().fckl_topk_kept_logits_workspace_bytes(N, d, V, K, chunk, dtype))
         elif kind == "topk_min":
             n = int(load().fckl_topk_workspace_bytes(N, d, V, K, chunk, dtype))
-        elif kind == "fused":
-            n = forward_backward_workspace_bytes(N, d, V, K, chunk, dtype)
         elif kind == "loss":
             n = workspace_bytes(N, d, V, K, chunk, dtype)
         else:
@@ -175,11 +166,11 @@ def _shape(H, W, idx, logp):
     return N, d, V, K
 
 
-def _ws_for(ws, N, d, V, K, chunk, dt, device, kind="loss"):
+def _ws_for(ws, N, d, V, K, chunk, dt, device):
     global _last_ws
     import weakref
     if ws is None:
-        ws = Workspace(N, d, V, K, chunk, dt, device, kind=kind)
+        ws = Workspace(N, d, V, K, chunk, dt, device)
         _last_ws = ws
     else:
         _last_ws = weakref.ref(ws)
@@ -224,20 +215,16 @@ def backward(H, W, idx, logp, lse, chunk, grad_scale=1.0, ws=None, stream=None, 
 
 
 def forward_backward(H, W, idx, logp, chunk, grad_scale=1.0, ws=None, stream=None, weight=None,
-                     row_loss=False, dH=None, dW=None, keep_logits=True):
+                     row_loss=False, dH=None, dW=None):
     """(loss, lse, dH, dW) — or (loss, lse, row_loss, dH, dW) with ``row_loss=True`` — from
-    one fckl_forward_backward call (each chunk's backward right after its forward).
-
-    ``keep_logits``: hold each chunk's fp32 logits from its forward for its backward instead
-    of recomputing them (needs a "fused" workspace; 4 * chunk * V bytes more). The outputs
-    are bitwise the same either way. With ``keep_logits=False`` only the "loss" part of the
-    workspace is handed to the library, which then recomputes."""
+    one fckl_forward_backward call: each chunk's backward right after its forward, from what
+    the forward kept in the gradient slab (no logits recomputed). Bitwise the outputs of
+    forward() then backward()."""
     import torch
     N, d, V, K = _shape(H, W, idx, logp)
     weight = _weight(weight, N)
     dt = _dtype_code(H)
-    ws = _ws_for(ws, N, d, V, K, chunk, dt, H.device, kind="fused" if keep_logits else "loss")
-    nbytes = ws.nbytes if keep_logits else min(ws.nbytes, workspace_bytes(N, d, V, K, chunk, dt))
+    ws = _ws_for(ws, N, d, V, K, chunk, dt, H.device)
     loss = torch.empty(1, dtype=torch.float32, device=H.device)
     lse = torch.empty(N, dtype=torch.float32, device=H.device)
     rl = torch.empty(N, dtype=torch.float32, device=H.device) if row_loss else None
@@ -247,7 +234,7 @@ def forward_backward(H, W, idx, logp, chunk, grad_scale=1.0, ws=None, stream=Non
         dW = torch.empty(V, d, dtype=torch.float32, device=H.device)
     st = load().fckl_forward_backward(_ptr(H), _ptr(W), dt, _ptr(idx), _ptr(logp), _ptr(weight), N, d, V, K,
                                       chunk, float(grad_scale), _ptr(loss), _ptr(lse), _ptr(rl), _ptr(dH),
-                                      _ptr(dW), ws.ptr, nbytes, _stream_ptr(stream))
+                                      _ptr(dW), ws.ptr, ws.nbytes, _stream_ptr(stream))
     if st != OK:
         raise FcklError(st, "fckl_forward_backward")
     return (loss, lse, rl, dH, dW) if row_loss else (loss, lse, dH, dW)

@@ -201,7 +201,6 @@ int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t 
 }
 
 // ------------------------------------------------------------------ plan / workspace
-constexpr int VOCAB_TILE = 256;  // BN of the two logits kernels
 constexpr int MAX_SPLITS = 4;    // K-splits of the dH product
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -216,7 +215,6 @@ struct Plan {
   int bn_d;        // N-tile of the dH / dW products
   size_t off_status, off_sidx, off_sp, off_S, off_T, off_pm, off_pl, off_pc, off_rowloss, off_G, off_dhp,
       off_Hb, off_Wb, total;
-  size_t off_Z, total_keep;  // the chunk's fp32 logits (row pitch ldG), kept by the one-call path
 };
 
 // N-tile of the dH and dW products (over d). 256 columns: an SM pair stages 128 each, two
@@ -265,8 +263,6 @@ Plan make_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
   p.off_Hb = dt == FCKL_F32 ? take(R * d * 2) : o;
   p.off_Wb = dt == FCKL_F32 ? take(static_cast<size_t>(V) * d * 2) : o;
   p.total = o;
-  p.off_Z = take(R * p.ldG * 4);
-  p.total_keep = o;
   return p;
 }
 
@@ -446,7 +442,8 @@ int chunk_prepare(Run& r, int64_t r0, int rows, const void** Hc) {
 }
 
 // Forward of one chunk: logits tiles -> per-tile (max, sum-exp, gathered sum) -> lse and loss.
-// With keep, the logits tiles are also stored (fp32) for the chunk's backward.
+// With keep, exp(z - tile max) is also stored (fp16) into the gradient slab for the chunk's
+// backward.
 int chunk_forward(Run& r, int64_t r0, int rows, const void* Hc, bool keep = false) {
   const Plan& pl = r.pl;
   const int d = pl.d;
@@ -471,7 +468,7 @@ int chunk_forward(Run& r, int64_t r0, int rows, const void* Hc, bool keep = fals
   p.pc = reinterpret_cast<float*>(w + pl.off_pc);
   p.ld_part = pl.rows_alloc;
   if (keep) {
-    if ((st = make_map(&p.tmC, w + pl.off_Z, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, pl.V, rows, uint64_t(pl.ldG) * 4, 32,
+    if ((st = make_map(&p.tmC, w + pl.off_G, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pl.V, rows, uint64_t(pl.ldG) * 2, 64,
                        32)))
       return st;
     p.c_xlim = pl.V;
@@ -524,30 +521,32 @@ int grad_recompute(Run& r, int64_t r0, int rows, const void* Hc) {
   return launch_tc<VOCAB_TILE, false, false, EPI_LOGIT_GRAD>(KIND_BWD_GRAD, r.di, pg, s, "bwd_logit_grad");
 }
 
-// The same G from the logits the chunk's forward kept (fp32, workspace offset off_Z).
+// The same G formed in place from what the chunk's forward kept in the slab (fp16
+// exp(z - tile max), with the tile maxima in pm).
 int grad_from_kept(Run& r, int64_t r0, int rows) {
   const Plan& pl = r.pl;
   const int V = pl.V;
   uint8_t* w = r.w;
   cudaStream_t s = r.s;
-  const int64_t units = int64_t(rows) * cdiv(V, GRAD_SEG);
+  const int64_t units = int64_t(rows) * cdiv(V, KG_SEG);
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(units, int64_t(r.di->sms) * 8)));
-  const float* Z = reinterpret_cast<const float*>(w + pl.off_Z);
+  __nv_bfloat16* G = reinterpret_cast<__nv_bfloat16*>(w + pl.off_G);
   const int* sidx = reinterpret_cast<const int*>(w + pl.off_sidx);
   const float* spp = reinterpret_cast<const float*>(w + pl.off_sp);
   const float* S = reinterpret_cast<const float*>(w + pl.off_S);
+  const float* pm = reinterpret_cast<const float*>(w + pl.off_pm);
   const float* lse = r.lse + r0;
   const float* wr = r.weight ? r.weight + r0 : nullptr;
   const float gsc = r.grad_scale;
-  __nv_bfloat16* Gb = reinterpret_cast<__nv_bfloat16*>(w + pl.off_G);
-  const int K = pl.K, ld = pl.ldG;
+  const int K = pl.K, ldp = pl.rows_alloc;
+  const int64_t ld = pl.ldG;
   return launch(KIND_BWD_GRAD_KEPT, s, "bwd_grad_from_logits", [&] {
-    logit_grad_kernel<<<grid, GRAD_THREADS, 0, s>>>(Z, ld, rows, V, K, sidx, spp, S, lse, wr, gsc, Gb);
+    logit_grad_kernel<<<grid, GRAD_THREADS, 0, s>>>(G, ld, rows, V, K, sidx, spp, S, lse, wr, gsc, pm, ldp);
   });
 }
 
-// Backward of one chunk: G from recomputed logits (or, with keep, from the logits the chunk's
-// forward stored), then dH_chunk = G W and dW (+)= G^T H_chunk.
+// Backward of one chunk: G from recomputed logits (or, with keep, from what the chunk's forward
+// kept in the slab), then dH_chunk = G W and dW (+)= G^T H_chunk.
 int chunk_backward(Run& r, int64_t r0, int rows, const void* Hc, bool keep = false) {
   const Plan& pl = r.pl;
   const int d = pl.d, V = pl.V;
@@ -700,10 +699,6 @@ size_t fckl_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype
   return make_plan(N, d, V, K, chunk, dtype).total;
 }
 
-size_t fckl_forward_backward_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype) {
-  if (check_shape(N, d, V, K, chunk, dtype) != FCKL_OK) return 0;
-  return make_plan(N, d, V, K, chunk, dtype).total_keep;
-}
 
 int fckl_forward(const void* H, const void* W, int dtype, const int32_t* idx, const float* logp,
                  const float* weight, int64_t N, int d, int V, int K, int chunk, float* loss, float* lse,
@@ -760,14 +755,13 @@ int fckl_forward_backward(const void* H, const void* W, int dtype, const int32_t
   r.grad_scale = grad_scale;
   r.dH = dH;
   r.dW = dW;
-  const bool keep = ws_bytes >= r.pl.total_keep;
   if ((st = run_begin(r, true))) return st;
   for (int64_t r0 = 0; r0 < N; r0 += r.pl.chunk) {
     const int rows = static_cast<int>(std::min<int64_t>(r.pl.chunk, N - r0));
     const void* Hc = nullptr;
     if ((st = chunk_prepare(r, r0, rows, &Hc))) return st;
-    if ((st = chunk_forward(r, r0, rows, Hc, keep))) return st;
-    if ((st = chunk_backward(r, r0, rows, Hc, keep))) return st;
+    if ((st = chunk_forward(r, r0, rows, Hc, true))) return st;
+    if ((st = chunk_backward(r, r0, rows, Hc, true))) return st;
   }
   return run_loss(r, loss);
 }
@@ -877,7 +871,7 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
         return st;
       p.c_xlim = V;
       p.c_ylim = rows;
-      st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_KEEP>(KIND_TOPK_LOGITS_KEEP, di, p, s, "topk_logits_keep");
+      st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_Z>(KIND_TOPK_LOGITS_KEEP, di, p, s, "topk_logits_keep");
     } else {
       st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_STATS>(KIND_TOPK_LOGITS, di, p, s, "topk_logits_stats");
     }

@@ -351,27 +351,41 @@ __global__ void __launch_bounds__(256) dh_reduce_kernel(const float* __restrict_
   }
 }
 
-// G from the chunk's logits as the forward kept them (fp32 Z, written by the EPI_FWD_KEEP
-// epilogue), instead of recomputing them: G = scale * w_n * (S_n exp(z - lse_n) - p at the
-// cached ids), rounded to bf16, with the same operations in the same order as the
-// EPI_LOGIT_GRAD epilogue, so G is bitwise the one the recomputing path forms.
-// HBM-bound (6 bytes per element): a unit is one position and GRAD_SEG columns; each thread
-// takes 8 adjacent columns per step (two 16-byte streaming loads of Z, one 16-byte store of
-// G), GRAD_STEPS steps 2048 columns apart. The row's ordered cache slots sit in shared memory
-// and each thread walks them with one cursor. Z and G share the row pitch ld (a multiple of
-// 8 elements); columns in [V, ld) of G are written as 0.
+// G, in place, from what the forward kept of the chunk's logits: the slab G holds
+// e = exp(z - m) as fp16 (EPI_FWD_KEEP), m being the logit's tile maximum (pm, one per row and
+// vocabulary tile). Each element becomes G = f * e - scale * w_n * p at the cached ids, with
+// f = scale * w_n * S_n * exp(m - lse_n), rounded to bf16 and written over e: the same
+// operations in the same order as the EPI_LOGIT_GRAD epilogue, so G is bitwise the one the
+// recomputing path forms. HBM-bound (4 bytes per element: 2 read, 2 written); a unit is one
+// position and KG_SEG columns, each thread takes 16 adjacent columns per step (two 16-byte
+// loads and stores at the same addresses), GRAD_STEPS steps 4096 columns apart, all loads
+// issued before the arithmetic (128 bytes in flight per thread). The row's ordered cache slots
+// sit in shared memory and each thread walks them with one cursor. Row pitch ld is a multiple
+// of 8 elements; columns in [V, ld) are written as 0.
+constexpr int KG_COLS = 16;
+constexpr int KG_SEG = GRAD_THREADS * KG_COLS * GRAD_STEPS;
 
 __global__ void __launch_bounds__(GRAD_THREADS) logit_grad_kernel(
-    const float* __restrict__ Z, int64_t ld, int rows, int V, int K, const int* __restrict__ sidx,
+    __nv_bfloat16* __restrict__ G, int64_t ld, int rows, int V, int K, const int* __restrict__ sidx,
     const float* __restrict__ sp, const float* __restrict__ S, const float* __restrict__ lse,
-    const float* __restrict__ wrow, float gscale, __nv_bfloat16* __restrict__ G) {
+    const float* __restrict__ wrow, float gscale, const float* __restrict__ pm, int ld_part) {
   __shared__ int s_ids[K_LIMIT];
   __shared__ float s_p[K_LIMIT];
-  const int segs = (V + GRAD_SEG - 1) / GRAD_SEG;
+  const int segs = (V + KG_SEG - 1) / KG_SEG;
   const int64_t units = static_cast<int64_t>(rows) * segs;
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
     const int row = static_cast<int>(u / segs);
     const int seg = static_cast<int>(u - static_cast<int64_t>(row) * segs);
+    __nv_bfloat16* gr = G + static_cast<int64_t>(row) * ld;
+    const int c0 = seg * KG_SEG + KG_COLS * static_cast<int>(threadIdx.x);
+    uint4 e[2 * GRAD_STEPS];
+#pragma unroll
+    for (int i = 0; i < GRAD_STEPS; ++i) {
+      const int c = c0 + i * GRAD_THREADS * KG_COLS;
+      // 8-column halves wholly past V are not read (the row pitch ends at a multiple of 8)
+      e[2 * i] = c < V ? *reinterpret_cast<const uint4*>(gr + c) : make_uint4(0u, 0u, 0u, 0u);
+      e[2 * i + 1] = c + 8 < V ? *reinterpret_cast<const uint4*>(gr + c + 8) : make_uint4(0u, 0u, 0u, 0u);
+    }
     __syncthreads();  // every thread is done with the previous unit's slots
     for (int k = threadIdx.x; k < K; k += GRAD_THREADS) {
       s_ids[k] = __ldg(sidx + static_cast<int64_t>(row) * K + k);
@@ -381,7 +395,6 @@ __global__ void __launch_bounds__(GRAD_THREADS) logit_grad_kernel(
     const float gs = __fmul_rn(gscale, wrow ? __ldg(wrow + row) : 1.f);
     const float a = __fmul_rn(gs, __ldg(S + row));
     const float nl = __fmul_rn(-__ldg(lse + row), LOG2E);
-    const int c0 = seg * GRAD_SEG + 8 * static_cast<int>(threadIdx.x);
     int lo = 0, hi = K;  // cursor: first slot whose id is >= c0
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
@@ -391,42 +404,37 @@ __global__ void __launch_bounds__(GRAD_THREADS) logit_grad_kernel(
         hi = mid;
     }
     int k = lo;
-    const float* zr = Z + static_cast<int64_t>(row) * ld;
-    __nv_bfloat16* gr = G + static_cast<int64_t>(row) * ld;
 #pragma unroll
     for (int i = 0; i < GRAD_STEPS; ++i) {
-      const int c = c0 + i * GRAD_THREADS * 8;
+      const int c = c0 + i * GRAD_THREADS * KG_COLS;
       if (c >= V) break;
-      float x[8];
-      if (c + 8 <= V) {
-        const float4 z0 = __ldcs(reinterpret_cast<const float4*>(zr + c));
-        const float4 z1 = __ldcs(reinterpret_cast<const float4*>(zr + c + 4));
-        x[0] = z0.x, x[1] = z0.y, x[2] = z0.z, x[3] = z0.w;
-        x[4] = z1.x, x[5] = z1.y, x[6] = z1.z, x[7] = z1.w;
-      } else {
+      const float f = tile_factor(a, __ldg(pm + static_cast<int64_t>(c / VOCAB_TILE) * ld_part + row), nl);
+      const __half* eh = reinterpret_cast<const __half*>(&e[2 * i]);
+      float x[KG_COLS];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) x[t] = c + t < V ? zr[c + t] : 0.f;
-      }
-#pragma unroll
-      for (int t = 0; t < 8; ++t) x[t] = grad_dense(x[t], a, nl);
+      for (int t = 0; t < KG_COLS; ++t) x[t] = grad_dense(f, eh[t]);
       while (k < K && s_ids[k] < c) ++k;
-      while (k < K && s_ids[k] < c + 8) {
+      while (k < K && s_ids[k] < c + KG_COLS) {
         const int pos = s_ids[k] - c;
         const float v = __fmul_rn(gs, s_p[k]);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) x[t] = (t == pos) ? __fsub_rn(x[t], v) : x[t];
+        for (int t = 0; t < KG_COLS; ++t) x[t] = (t == pos) ? __fsub_rn(x[t], v) : x[t];
         ++k;
       }
-      if (c + 8 > V) {
+      if (c + KG_COLS > V) {
 #pragma unroll
-        for (int t = 0; t < 8; ++t) x[t] = c + t < V ? x[t] : 0.f;
+        for (int t = 0; t < KG_COLS; ++t) x[t] = c + t < V ? x[t] : 0.f;
       }
-      uint4 w;
-      w.x = pack_bf16x2(x[0], x[1]);
-      w.y = pack_bf16x2(x[2], x[3]);
-      w.z = pack_bf16x2(x[4], x[5]);
-      w.w = pack_bf16x2(x[6], x[7]);
-      *reinterpret_cast<uint4*>(gr + c) = w;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        if (c + 8 * hh >= V) break;
+        uint4 w;
+        w.x = pack_bf16x2(x[8 * hh + 0], x[8 * hh + 1]);
+        w.y = pack_bf16x2(x[8 * hh + 2], x[8 * hh + 3]);
+        w.z = pack_bf16x2(x[8 * hh + 4], x[8 * hh + 5]);
+        w.w = pack_bf16x2(x[8 * hh + 6], x[8 * hh + 7]);
+        *reinterpret_cast<uint4*>(gr + c + 8 * hh) = w;
+      }
     }
   }
 }

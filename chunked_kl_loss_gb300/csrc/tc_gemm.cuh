@@ -13,14 +13,20 @@
 // chosen by the host so that concurrently running CTAs share operand tiles in L2.
 //
 // Epilogues (the steps of the method that follow each projection):
-//   EPI_FWD_STATS : per-row online max / sum-exp over the tile's vocabulary columns and
-//                   the gather of the logits at the teacher's cached ids; writes one
-//                   (m, l, c) triple per row and vocabulary tile ("Fused, chunked KL loss":
-//                   fold the chunk's logits into the running loss, then drop them)
-//   EPI_FWD_KEEP  : EPI_FWD_STATS that also stores the fp32 logits tile with TMA, so that
-//                   the chunk's backward can form G from them instead of recomputing them
+//   EPI_FWD_STATS : per row, the tile's maximum m over its vocabulary columns (first pass
+//                   over the accumulator), the gather of the logits at the teacher's cached
+//                   ids, and sum_v exp(z_v - m) (second pass); writes one (m, l, c) triple per
+//                   row and vocabulary tile ("Fused, chunked KL loss": fold the chunk's
+//                   logits into the running loss, then drop them)
+//   EPI_FWD_KEEP  : EPI_FWD_STATS that also stores e = exp(z - m) as fp16 with TMA into the
+//                   chunk's gradient slab, so that the chunk's backward can form G from it
+//                   in place instead of recomputing the logits
+//   EPI_FWD_Z     : EPI_FWD_STATS that also stores the fp32 logits with TMA (teacher top-K
+//                   builder: its second pass compares exact logits)
 //   EPI_LOGIT_GRAD: G = scale * w_n * (S_n exp(z - lse_n) - p at the cached ids), rounded
-//                   to bf16 and stored with TMA (the backward pass recomputes the chunk)
+//                   to bf16 and stored with TMA (the backward pass recomputes the chunk);
+//                   exp(z - lse_n) is formed as exp(m - lse_n) * fp16(exp(z - m)) with the
+//                   tile maximum m, the same values the EPI_FWD_KEEP path keeps
 //   EPI_STORE_F32 : fp32 tile stored, or reduce-added, with TMA (dH partials, dW)
 //   EPI_TOPK_COLLECT: appends every logit at or above the row's threshold, with its token
 //                   id, to the row's candidate list (teacher top-K cache builder)
@@ -29,6 +35,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <climits>
 #include <cstdint>
 
@@ -38,6 +45,7 @@ namespace fckl {
 
 constexpr int BM = 128;  // rows of A per CTA
 constexpr int BK = 64;   // K per pipeline stage (one 128-byte swizzle row of bf16)
+constexpr int VOCAB_TILE = 256;  // vocabulary columns per tile of the logits kernels (their BN)
 constexpr int EPI_WARPS = 4;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
@@ -47,7 +55,7 @@ constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;
 constexpr float LOG2E = 1.4426950408889634f;
 
 enum : unsigned { ST_BAD_INDEX = 1u, ST_TIMEOUT = 2u, ST_CAPACITY = 4u };
-enum { EPI_FWD_STATS = 0, EPI_LOGIT_GRAD = 1, EPI_STORE_F32 = 2, EPI_TOPK_COLLECT = 3, EPI_FWD_KEEP = 4 };
+enum { EPI_FWD_STATS = 0, EPI_LOGIT_GRAD = 1, EPI_STORE_F32 = 2, EPI_TOPK_COLLECT = 3, EPI_FWD_KEEP = 4, EPI_FWD_Z = 5 };
 
 struct Sched {
   int m_blocks, n_blocks, k_blocks;
@@ -185,11 +193,26 @@ __device__ __forceinline__ void sub32(float (&x)[32], int pos, float v) {
   for (int t = 0; t < 32; ++t) x[t] = (t == pos) ? __fsub_rn(x[t], v) : x[t];
 }
 
-// One element of G before rounding, with every operation rounded on its own (no contraction
-// into FMAs), so that a kernel forming G from stored logits gets the same bits as the
-// recomputing epilogue: a = scale * w_n * S_n, nl = -lse_n * log2(e).
-__device__ __forceinline__ float grad_dense(float z, float a, float nl) {
-  return __fmul_rn(a, ex2_approx(fmaf(z, LOG2E, nl)));
+// The dense part of G, in steps that every path takes identically (each operation rounded
+// on its own, no contraction into FMAs), so that G formed from the kept values has the bits
+// of G formed from recomputed logits. With the tile maximum m (ml = m * log2(e)):
+//   e = exp(z - m), kept as fp16 (relative rounding 2^-11, finer than G's own bf16 2^-9)
+//   f = a * exp(m - lse_n),  a = scale * w_n * S_n,  nl = -lse_n * log2(e)
+//   G_dense = f * e
+__device__ __forceinline__ float exp_in_tile(float z, float ml) { return ex2_approx(fmaf(z, LOG2E, -ml)); }
+__device__ __forceinline__ float tile_factor(float a, float m, float nl) {
+  return __fmul_rn(a, ex2_approx(fmaf(m, LOG2E, nl)));
+}
+__device__ __forceinline__ float grad_dense(float f, __half e) { return __fmul_rn(f, __half2float(e)); }
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ float max32(const float (&x)[32]) {
+  float m = x[0];
+#pragma unroll
+  for (int t = 1; t < 32; ++t) m = fmaxf(m, x[t]);
+  return m;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -423,7 +446,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       const int row0 = mb * BM * CG + static_cast<int>(rank) * BM + 32 * q;  // first row of this warp
       const int row = row0 + lane;
 
-      if constexpr (EPI == EPI_FWD_STATS || EPI == EPI_FWD_KEEP || EPI == EPI_LOGIT_GRAD) {
+      if constexpr (EPI == EPI_FWD_STATS || EPI == EPI_FWD_KEEP || EPI == EPI_FWD_Z || EPI == EPI_LOGIT_GRAD) {
         const bool valid = row < p.rows_valid;
         const int v0 = nb * BN;
         const int* ids = p.sidx + static_cast<size_t>(valid ? row : 0) * p.K;
@@ -433,18 +456,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           k = lower_bound_ids(ids, p.K, v0);
           nxt = k < p.K ? __ldg(ids + k) : INT_MAX;
         }
-        if constexpr (EPI == EPI_FWD_STATS || EPI == EPI_FWD_KEEP) {
+        if constexpr (EPI == EPI_FWD_STATS || EPI == EPI_FWD_KEEP || EPI == EPI_FWD_Z) {
           if (!warp_wait_phase(&tfull[acc], use & 1u, abort_flag, p.status)) break;
           tc_fence_after();
-          float m = -INFINITY, l = 0.f, c = 0.f;
+          // pass 1: the tile maximum (columns past V excluded) and the gathered sum
+          float m = -INFINITY, c = 0.f;
 #pragma unroll 1
-          for (int j = 0; j < BN / 32; ++j, ++ecnt) {
+          for (int j = 0; j < BN / 32; ++j) {
             float x[32];
             __syncwarp();
             tmem_ld32(taddr + 32 * j, x);
-            if (j == BN / 32 - 1) release_acc(acc);
             const int cb = v0 + 32 * j;
-            if constexpr (EPI == EPI_FWD_KEEP) {
+            if constexpr (EPI == EPI_FWD_Z) {
               // stage the raw logits (32 rows x 32 columns, 128-byte swizzle) and store them
               uint8_t* buf = ebuf0 + (ecnt & 1u) * EPI_BUF_BYTES;
               if (ecnt >= 2 && lane == 0) bulk_wait_read<1>();
@@ -461,6 +484,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 if (cb < p.c_xlim && row0 < p.c_ylim) tma_store_2d(&p.tmC, buf, cb, row0);
                 bulk_commit();
               }
+              ++ecnt;
             }
             if (cb + 32 > p.V) {
 #pragma unroll
@@ -472,16 +496,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
               ++k;
               nxt = k < p.K ? __ldg(ids + k) : INT_MAX;
             }
-            float cm = x[0];
+            m = fmaxf(m, max32(x));
+          }
+          // pass 2: sum of exp(z - m); EPI_FWD_KEEP also stores fp16 exp(z - m), 64-column boxes
+          const float ml = __fmul_rn(m, LOG2E);
+          float l = 0.f;
+#pragma unroll 1
+          for (int jj = 0; jj < BN / 64; ++jj) {
+            uint8_t* buf = ebuf0 + (ecnt & 1u) * EPI_BUF_BYTES;
+            if constexpr (EPI == EPI_FWD_KEEP) {
+              if (ecnt >= 2 && lane == 0) bulk_wait_read<1>();
+              __syncwarp();
+            }
 #pragma unroll
-            for (int t = 1; t < 32; ++t) cm = fmaxf(cm, x[t]);
-            const float nm = fmaxf(m, cm);
-            const float nml = nm * LOG2E;
-            float s = 0.f;
+            for (int h = 0; h < 2; ++h) {
+              const int j = 2 * jj + h;
+              float x[32];
+              __syncwarp();
+              tmem_ld32(taddr + 32 * j, x);
+              if (j == BN / 32 - 1) release_acc(acc);
+              const int cb = v0 + 32 * j;
+              if (cb + 32 > p.V) {
 #pragma unroll
-            for (int t = 0; t < 32; ++t) s += ex2_approx(fmaf(x[t], LOG2E, -nml));
-            l = fmaf(l, ex2_approx((m - nm) * LOG2E), s);
-            m = nm;
+                for (int t = 0; t < 32; ++t)
+                  if (cb + t >= p.V) x[t] = -INFINITY;
+              }
+#pragma unroll
+              for (int t = 0; t < 32; ++t) {
+                x[t] = exp_in_tile(x[t], ml);
+                l += x[t];
+              }
+              if constexpr (EPI == EPI_FWD_KEEP) {
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                  uint4 w;
+                  w.x = pack_f16x2(x[8 * cc + 0], x[8 * cc + 1]);
+                  w.y = pack_f16x2(x[8 * cc + 2], x[8 * cc + 3]);
+                  w.z = pack_f16x2(x[8 * cc + 4], x[8 * cc + 5]);
+                  w.w = pack_f16x2(x[8 * cc + 6], x[8 * cc + 7]);
+                  const int chunk16 = (4 * h + cc) ^ (lane & 7);
+                  *reinterpret_cast<uint4*>(buf + lane * 128 + chunk16 * 16) = w;
+                }
+              }
+            }
+            if constexpr (EPI == EPI_FWD_KEEP) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                const int sx = v0 + 64 * jj;
+                if (sx < p.c_xlim && row0 < p.c_ylim) tma_store_2d(&p.tmC, buf, sx, row0);
+                bulk_commit();
+              }
+              ++ecnt;
+            }
           }
           if (valid) {
             const size_t o = static_cast<size_t>(nb) * p.ld_part + row;
@@ -495,6 +562,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           const float nl = valid ? __fmul_rn(-__ldg(p.lse + row), LOG2E) : 0.f;
           if (!warp_wait_phase(&tfull[acc], use & 1u, abort_flag, p.status)) break;
           tc_fence_after();
+          // pass 1: the tile maximum, as the forward took it
+          float m = -INFINITY;
+#pragma unroll 1
+          for (int j = 0; j < BN / 32; ++j) {
+            float x[32];
+            __syncwarp();
+            tmem_ld32(taddr + 32 * j, x);
+            const int cb = v0 + 32 * j;
+            if (cb + 32 > p.V) {
+#pragma unroll
+              for (int t = 0; t < 32; ++t)
+                if (cb + t >= p.V) x[t] = -INFINITY;
+            }
+            m = fmaxf(m, max32(x));
+          }
+          const float ml = __fmul_rn(m, LOG2E);
+          const float f = tile_factor(a, m, nl);
 #pragma unroll 1
           for (int jj = 0; jj < BN / 64; ++jj, ++ecnt) {
             uint8_t* buf = ebuf0 + (ecnt & 1u) * EPI_BUF_BYTES;
@@ -509,7 +593,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
               if (j == BN / 32 - 1) release_acc(acc);
               const int cb = v0 + 32 * j;
 #pragma unroll
-              for (int t = 0; t < 32; ++t) x[t] = grad_dense(x[t], a, nl);
+              for (int t = 0; t < 32; ++t) x[t] = grad_dense(f, __float2half_rn(exp_in_tile(x[t], ml)));
               while (nxt < cb + 32) {
                 sub32(x, nxt - cb, __fmul_rn(gs, __ldg(pr + k)));
                 ++k;

@@ -14,9 +14,9 @@
  *
  * The sequence is walked one chunk of positions at a time: the forward pass projects
  * a chunk, folds it into the running loss and drops it; the backward pass recomputes
- * the chunk's logits to form G (the one-call path may instead keep the chunk's logits from
- * its forward, see fckl_forward_backward_workspace_bytes). Only one chunk's slabs (G, and
- * the kept logits) are ever held.
+ * the chunk's logits to form G (the one-call path instead keeps, in the gradient slab itself,
+ * what its backward needs of the chunk's logits, see fckl_forward_backward). Only one chunk x V
+ * slab is ever held.
  *
  * Conventions for every call below
  *  - All arrays are dense and row-major. "device" pointers are CUDA device memory of the
@@ -75,14 +75,6 @@ typedef enum { FCKL_BF16 = 0, FCKL_F32 = 1 } fckl_dtype;
  * position; 0 if the shape is outside the limits. */
 size_t fckl_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
 
-/* Workspace with which fckl_forward_backward keeps each chunk's logits between its forward
- * and its backward: fckl_workspace_bytes() plus one chunk of fp32 logits (chunk x V, rows
- * padded to 256 and to a multiple of 8 columns). Not an operation of the pages' method but
- * a trade of memory for compute that the one-call path allows: the logits of a chunk are
- * recomputed in the backward there only because the forward drops them ("Fused, chunked KL
- * loss"); here one chunk's worth is held, still independent of N. 0 outside the limits. */
-size_t fckl_forward_backward_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
-
 /* Forward pass.
  *   loss     : device fp32 [1]  <- sum over positions of the per-position KL (a SUM, not a mean)
  *   lse      : device fp32 [N]  <- log-partition of every position, kept for fckl_backward
@@ -109,12 +101,16 @@ int fckl_backward(const void* H, const void* W, int dtype,
 /* Forward and backward in one call, chunk by chunk: each chunk's backward runs right after
  * its forward (lse_n depends on position n alone), so the chunk's cache slots are ordered
  * once and its hidden states are re-read while still in L2. Outputs as fckl_forward and
- * fckl_backward (row_loss may be NULL).
- * Workspace: at least fckl_workspace_bytes(); with ws_bytes >=
- * fckl_forward_backward_workspace_bytes() the forward also stores each chunk's fp32 logits
- * and the backward forms G from them instead of recomputing the logits (one product of the
- * four per chunk saved, for 4 * chunk * V more bytes of workspace). Both ways compute the
- * same operations on the same values: the outputs are bitwise identical. */
+ * fckl_backward (row_loss may be NULL); same workspace size.
+ * The chunk's logits are not recomputed: its forward stores e = exp(z - m) as fp16 into the
+ * gradient slab (m: the logit's 256-column tile maximum, kept with the softmax statistics)
+ * and its backward turns the slab into G in place, G = S_n exp(m - lse_n) e - p at the cached
+ * ids (times the weight and grad_scale). This saves one of the four products per chunk and
+ * needs no memory beyond the slab. fckl_backward forms G from recomputed logits with the same
+ * operations (tile maximum, fp16 e, the same products and roundings), so the two calls give
+ * bitwise identical outputs. Not an operation of the pages' method: their backward recomputes
+ * each chunk only because their forward drops it ("Fused, chunked KL loss"); here the backward
+ * directly follows the forward. */
 int fckl_forward_backward(const void* H, const void* W, int dtype,
                           const int32_t* idx, const float* logp, const float* weight,
                           int64_t N, int d, int V, int K, int chunk, float grad_scale,

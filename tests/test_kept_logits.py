@@ -1,10 +1,12 @@
-"""The one-call path that keeps each chunk's logits (fckl_forward_backward with a "fused"
-workspace) against the oracle, and against the recomputing one-call path bit for bit.
+"""The one call (fckl_forward_backward), whose backward forms G in place from what each
+chunk's forward kept in the gradient slab (fp16 exp(z - tile max)), against the oracle, and
+against the separate calls (fckl_forward, then fckl_backward recomputing the logits) bit for
+bit.
 
-Keeping the logits changes where z comes from (the forward's own fp32 tile, stored, instead
-of the same product computed again), not what is computed from it, so every output must be
-identical to the recomputing path's. The profile counters show which kernels ran, so the
-comparison cannot pass by running the same path twice.
+Both paths take the same steps from the same logits (tile maximum, fp16 e, the same products
+and roundings); only where the logits come from differs (the forward's own tile, kept, or the
+same product computed again), so every output must be identical. The profile counters show
+which kernels ran, so the comparison cannot pass by running the same path twice.
 """
 import numpy as np
 import pytest
@@ -30,19 +32,25 @@ def to_dev(x, dtype):
 
 
 def run_both(fckl, x, chunk, dtype, grad_scale=1.0, weight=None):
-    """(kept, recomputed) outputs of forward_backward, each with the kernels it launched."""
+    """(kept, recomputed) outputs: the one call, and the separate calls; each with the kernels
+    it launched."""
     H, W, idx, logp = to_dev(x, dtype)
     N, d = H.shape
     V, K = W.shape[0], idx.shape[1]
     dt = fckl.F32 if dtype == "f32" else fckl.BF16
     wd = torch.from_numpy(weight).cuda() if weight is not None else None
     out = []
-    for kind in ("fused", "loss"):
-        ws = fckl.Workspace(N, d, V, K, chunk, dt, kind=kind)
+    for one_call in (True, False):
+        ws = fckl.Workspace(N, d, V, K, chunk, dt)
         fckl.profile_enable(True)
         fckl.profile_read()
-        res = fckl.forward_backward(H, W, idx, logp, chunk, grad_scale=grad_scale, ws=ws, weight=wd,
-                                    row_loss=True)
+        if one_call:
+            res = fckl.forward_backward(H, W, idx, logp, chunk, grad_scale=grad_scale, ws=ws, weight=wd,
+                                        row_loss=True)
+        else:
+            loss, lse, rl = fckl.forward(H, W, idx, logp, chunk, ws=ws, weight=wd, row_loss=True)
+            dH, dW = fckl.backward(H, W, idx, logp, lse, chunk, grad_scale=grad_scale, ws=ws, weight=wd)
+            res = (loss, lse, rl, dH, dW)
         prof = fckl.profile_read()
         fckl.profile_enable(False)
         assert fckl.check(ws) == fckl.OK
@@ -127,21 +135,26 @@ def test_kept_logits_llama_vocab(fckl):
     assert_oracle(kept, x, 256)
 
 
-def test_workspace_kind_decides_the_path(fckl):
-    """A caller workspace of the "fused" size keeps the logits; keep_logits=False hands the
-    library only the smaller size and it recomputes; outputs equal."""
+def test_one_call_needs_no_workspace_beyond_the_slab(fckl):
+    """The kept values live in the gradient slab: a workspace of fckl_workspace_bytes runs the
+    one call, and one byte less is refused before anything is launched."""
     x = synthetic.make_inputs(200, 128, 2500, 10, dtype="bf16", seed=44)
     H, W, idx, logp = to_dev(x, "bf16")
-    ws = fckl.Workspace(200, 128, 2500, 10, 64, fckl.BF16, kind="fused")
-    assert ws.nbytes == fckl.forward_backward_workspace_bytes(200, 128, 2500, 10, 64, fckl.BF16)
+    ws = fckl.Workspace(200, 128, 2500, 10, 64, fckl.BF16)
+    assert ws.nbytes == fckl.workspace_bytes(200, 128, 2500, 10, 64, fckl.BF16)
     fckl.profile_enable(True)
     fckl.profile_read()
-    a = fckl.forward_backward(H, W, idx, logp, 64, ws=ws)
-    pa = fckl.profile_read()
-    b = fckl.forward_backward(H, W, idx, logp, 64, ws=ws, keep_logits=False)
-    pb = fckl.profile_read()
+    fckl.forward_backward(H, W, idx, logp, 64, ws=ws)
+    prof = fckl.profile_read()
     fckl.profile_enable(False)
     assert fckl.check(ws) == fckl.OK
-    assert pa["bwd_grad_from_logits"][1] == 4 and pa["bwd_logit_grad"][1] == 0
-    assert pb["bwd_grad_from_logits"][1] == 0 and pb["bwd_logit_grad"][1] == 4
-    assert_bitwise(a, b)
+    assert prof["bwd_grad_from_logits"][1] == 4 and prof["bwd_logit_grad"][1] == 0
+
+    class Short:
+        tensor = ws.tensor
+        nbytes = ws.nbytes - 1
+        ptr = ws.ptr
+    n0 = fckl.launch_count()
+    with pytest.raises(fckl.FcklError):
+        fckl.forward_backward(H, W, idx, logp, 64, ws=Short())
+    assert fckl.launch_count() == n0

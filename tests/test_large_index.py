@@ -30,7 +30,7 @@ def test_more_than_2_31_elements_in_H_and_dH(fckl):
     W = torch.from_numpy(x["W"]).to(dev).to(torch.bfloat16)
     idx = torch.from_numpy(x["idx"]).to(dev)
     logp = torch.from_numpy(x["logp"]).to(dev)
-    ws = fckl.Workspace(N, D, V, K, CHUNK, fckl.BF16, kind="fused")
+    ws = fckl.Workspace(N, D, V, K, CHUNK, fckl.BF16)
     loss, lse, rl, dH, dW = fckl.forward_backward(H, W, idx, logp, CHUNK, ws=ws, row_loss=True)
     assert fckl.check(ws) == fckl.OK
 

@@ -1,6 +1,5 @@
 """GPU parity at the full workload sizes, in the launch configuration bench.py times (one
-fckl_forward_backward call with a "fused" workspace: each chunk's logits kept from its
-forward for its backward).
+fckl_forward_backward call: each chunk's backward forms G from what its forward kept).
 
 At these sizes the oracle cannot run the whole problem in a test, so it checks what it can
 compute one position at a time — lse_n, the per-position loss and the dH row of sampled
@@ -31,7 +30,7 @@ def test_full_size_sampled_rows_and_properties(fckl, name):
     W = torch.from_numpy(x["W"]).to(dev).to(torch.bfloat16)
     idx = torch.from_numpy(x["idx"]).to(dev)
     logp = torch.from_numpy(x["logp"]).to(dev)
-    ws = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, fckl.BF16, kind="fused")
+    ws = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, fckl.BF16)
     loss, lse, rl, dH, dW = fckl.forward_backward(H, W, idx, logp, w.chunk, ws=ws, row_loss=True)
     assert fckl.check(ws) == fckl.OK
     if name == "n32768_d3072_v128256":
