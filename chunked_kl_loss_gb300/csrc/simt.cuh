@@ -12,8 +12,9 @@ namespace fckl {
 
 constexpr int PRE_WARPS = 4;
 constexpr int K_LIMIT = 1024;
-// Kernels that stream a chunk's kept fp32 logits: threads per block, steps of 8 columns per
-// thread, and the columns of one unit (one position).
+// Kernels that stream what a chunk's forward kept (the top-K builder's fp32 logits, the one
+// call's fp16 e): threads per block, steps per thread, and the columns of one unit of
+// topk_collect_kernel (one position, 8 columns per thread and step).
 constexpr int GRAD_THREADS = 256;
 constexpr int GRAD_STEPS = 4;
 constexpr int GRAD_SEG = GRAD_THREADS * 8 * GRAD_STEPS;
@@ -216,7 +217,7 @@ __global__ void __launch_bounds__(256) topk_threshold_kernel(const float* __rest
 // the recomputing collect epilogue, so the candidate set is the same (the append order is
 // not fixed in either; the select step orders the candidates fully). HBM-bound (4 bytes per
 // element); units of one position and GRAD_SEG columns, 8 adjacent columns per thread and
-// step, as in logit_grad_kernel.
+// step, all of a thread's loads issued before its compares.
 __global__ void __launch_bounds__(GRAD_THREADS) topk_collect_kernel(
     const float* __restrict__ Z, int64_t ld, int rows, int V, const float* __restrict__ thr,
     int* __restrict__ cnt, int* __restrict__ cand_v, float* __restrict__ cand_z, int cmax) {
