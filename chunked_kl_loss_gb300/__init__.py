@@ -244,22 +244,30 @@ def _autograd_function():
     import torch
 
     class FusedChunkedKL(torch.autograd.Function):
-        """Autograd wrapper: the forward keeps lse only; the backward recomputes each chunk's
-        logits (fckl_backward) with the upstream gradient as grad_scale. Reading the upstream
-        gradient synchronises with the device once per backward."""
+        """Autograd wrapper. When H or W needs a gradient, the forward runs the one call
+        (fckl_forward_backward with grad_scale 1) and holds dH and dW; the backward multiplies
+        them by the upstream gradient on the device (fp32 product, one rounding to H's dtype;
+        no host synchronisation; exact when the upstream gradient is 1). Without gradients the
+        forward runs fckl_forward alone."""
 
         @staticmethod
         def forward(ctx, H, W, idx, logp, chunk, weight):
-            loss, lse = forward(H, W, idx, logp, chunk, weight=weight)
-            ctx.save_for_backward(H, W, idx, logp, lse, weight)
-            ctx.chunk = chunk
+            if ctx.needs_input_grad[0] or ctx.needs_input_grad[1]:
+                loss, _, dH, dW = forward_backward(H, W, idx, logp, chunk, weight=weight)
+                ctx.grads = (dH, dW)
+            else:
+                loss, _ = forward(H, W, idx, logp, chunk, weight=weight)
+                ctx.grads = None
             return loss[0]
 
         @staticmethod
         def backward(ctx, g):
-            H, W, idx, logp, lse, weight = ctx.saved_tensors
-            dH, dW = backward(H, W, idx, logp, lse, ctx.chunk, grad_scale=float(g), weight=weight)
-            return dH, dW, None, None, None, None
+            dH, dW = ctx.grads
+            ctx.grads = None
+            g32 = g.float()
+            gH = (dH.float() * g32).to(dH.dtype) if ctx.needs_input_grad[0] else None
+            gW = dW * g32 if ctx.needs_input_grad[1] else None
+            return gH, gW, None, None, None, None
 
     return FusedChunkedKL
 

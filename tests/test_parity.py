@@ -191,6 +191,33 @@ def test_autograd_wrapper(fckl):
     assert np.abs(gW - r_dW).max() <= GRAD_TOL * np.abs(r_dW).max()
 
 
+def test_autograd_wrapper_paths(fckl):
+    """Upstream gradient 1: the gradients are the one call's outputs bit for bit. Only W
+    needing a gradient works. Without gradients only the forward kernels run."""
+    N, d, V, K, chunk = 200, 128, 2048, 20, 64
+    x = synthetic.make_inputs(N, d, V, K, dtype="bf16", seed=13)
+    H, W, idx, logp = to_dev(x, "bf16")
+    loss_ref, _, dH_ref, dW_ref = fckl.forward_backward(H, W, idx, logp, chunk)
+    Hg, Wg = H.clone().requires_grad_(True), W.clone().requires_grad_(True)
+    loss = fckl.fused_chunked_kl(Hg, Wg, idx, logp, chunk)
+    loss.backward()
+    assert torch.equal(loss.detach(), loss_ref[0])
+    assert torch.equal(Hg.grad, dH_ref)
+    assert torch.equal(Wg.grad, dW_ref.to(torch.bfloat16))
+    Wg2 = W.clone().requires_grad_(True)
+    fckl.fused_chunked_kl(H, Wg2, idx, logp, chunk).backward()
+    assert torch.equal(Wg2.grad, dW_ref.to(torch.bfloat16))
+    fckl.profile_enable(True)
+    fckl.profile_read()
+    with torch.no_grad():
+        l3 = fckl.fused_chunked_kl(H, W, idx, logp, chunk)
+    prof = fckl.profile_read()
+    fckl.profile_enable(False)
+    assert torch.equal(l3, loss_ref[0])
+    ran = {k for k, (_, n) in prof.items() if n > 0}
+    assert "fwd_logits_lse" in ran and not ran & {"bwd_dH_gemm", "bwd_dW_gemm", "fwd_logits_keep"}
+
+
 def test_bounded_wait_times_out_and_context_survives(fckl):
     """Failure detection without a fault: a wait that nothing satisfies gives up, the status
     word says so, and the next call on the same context works."""
