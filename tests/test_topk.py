@@ -148,3 +148,33 @@ def test_topk_kept_and_recomputed_logits_agree(fckl, N, d, V, K, chunk):
     assert torch.equal(out[True][1], out[False][1])
     idx, logp = (t.cpu().numpy() for t in out[True])
     assert_topk_parity(idx.astype(np.int64), logp.astype(np.float64), Ht, Wt, K)
+
+
+@pytest.mark.parametrize("keep", [True, False])
+def test_topk_candidate_overflow_is_reported(fckl, keep):
+    """Every token ties (identical rows of Wt), so all V = 5000 logits of a position reach the
+    threshold and overflow the 2048-slot candidate buffer: the status reports FCKL_ERR_CAPACITY,
+    nothing is written out of bounds (the K outputs are still distinct tokens with the right
+    log-probability, -log V, since any K tied tokens are a top-K), and the next call on the same
+    context is exact again."""
+    rng = np.random.default_rng(25)
+    N, d, V, K = 64, 128, 5000, 10
+    Ht = synthetic.round_bf16(rng.standard_normal((N, d), dtype=np.float32))
+    row = synthetic.round_bf16(rng.standard_normal((1, d), dtype=np.float32) / 8)
+    Wt = np.repeat(row, V, axis=0)
+    dev = torch.device("cuda")
+    H = torch.from_numpy(Ht).to(dev).to(torch.bfloat16)
+    W = torch.from_numpy(Wt).to(dev).to(torch.bfloat16)
+    idx, logp = fckl.teacher_topk(H, W, K, 64, keep_logits=keep)
+    assert fckl.check(raise_on_error=False) == fckl.ERR_CAPACITY
+    idx, logp = idx.cpu().numpy(), logp.cpu().numpy()
+    assert idx.min() >= 0 and idx.max() < V
+    for n in range(N):
+        assert len(set(idx[n].tolist())) == K
+    assert np.abs(logp + np.log(V)).max() <= 1e-3
+    # the context and the library state are intact
+    rng2 = np.random.default_rng(26)
+    Ht2 = synthetic.round_bf16(rng2.standard_normal((N, d), dtype=np.float32))
+    Wt2 = synthetic.round_bf16(rng2.standard_normal((V, d), dtype=np.float32) / 4)
+    i2, l2 = run_topk(fckl, Ht2, Wt2, K, 64)
+    assert_topk_parity(i2, l2, Ht2, Wt2, K)
