@@ -102,8 +102,17 @@ def oracle_sample_size(w, target_s=15.0):
     return max(8, min(w.N, guess))
 
 
+def calibrated_sample_size(w, seed, target_s):
+    """Rows of an oracle sample taking about target_s seconds on this host: a short timed run
+    of the oracle itself sets the rate (cost is linear in rows)."""
+    n0 = max(8, min(w.N, oracle_sample_size(w, target_s=1.0)))
+    x, W = cpu_inputs(w, seed, n0)
+    t0 = sample_rows_oracle(w, x, W, n0)
+    return max(8, min(w.N, int(n0 * target_s / max(t0, 1e-3))))
+
+
 def cpu_baseline(w, seed):
-    n = oracle_sample_size(w)
+    n = calibrated_sample_size(w, seed, target_s=15.0)
     x, W = cpu_inputs(w, seed, n)
     t = sample_rows_oracle(w, x, W, n)
     return {"value": n / t, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
@@ -539,12 +548,17 @@ def topk_bench(args):
                               for k, v in prof.items() if v[1]}}
     if not args.no_cpu_baseline:
         from oracle import fckl_oracle as orc
-        n = max(8, int(8.0 * 100e9 / (2.0 * w.d * w.V)))  # ~8 s at ~100 GFLOP/s fp64
-        Hs = synthetic.round_bf16(synthetic.hidden_states(n, w.d, args.seed + 10))
         Ws = synthetic.round_bf16(synthetic.output_projection(w.V, w.d, args.seed + 11))
-        t0 = time.perf_counter()
-        orc.teacher_topk(Hs, Ws, w.K, chunk=w.chunk)
-        t = time.perf_counter() - t0
+
+        def timed(n):
+            Hs = synthetic.round_bf16(synthetic.hidden_states(n, w.d, args.seed + 10))
+            t0 = time.perf_counter()
+            orc.teacher_topk(Hs, Ws, w.K, chunk=w.chunk)
+            return time.perf_counter() - t0
+
+        n0 = max(8, int(1.0 * 100e9 / (2.0 * w.d * w.V)))  # a short run sets the host's rate
+        n = max(8, min(w.N, int(n0 * 15.0 / max(timed(n0), 1e-3))))  # about 15 s
+        t = timed(n)
         line["cpu_baseline"] = {"value": n / t, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
                                 "sample": f"fp64 oracle top-{w.K} cache of the first {n} of {w.N} positions "
                                           f"(full V={w.V}, d={w.d}), {t:.1f} s"}
