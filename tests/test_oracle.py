@@ -355,3 +355,34 @@ def test_teacher_generator_terminates_when_K_is_close_to_V():
         idx, logp = synthetic.teacher_cache(N, V, K, seed=1)
         assert all(len(set(r)) == K for r in idx.tolist()) and idx.max() < V
     assert time.time() - t0 < 10
+
+
+def test_empty_row_and_one_hot_row_closed_forms():
+    """A position whose slots are all empty carries no teacher mass: no loss and no gradient.
+    A position whose mass is one token (p = 1) has the cross-entropy -log q_i = lse - z_i as
+    its loss and G = softmax(z) - e_i, checked against scipy's log-softmax."""
+    rng = np.random.default_rng(17)
+    N, d, V, K = 6, 16, 50, 4
+    H = rng.standard_normal((N, d))
+    W = rng.standard_normal((V, d)) / 4
+    idx = np.stack([rng.choice(V, K, replace=False) for _ in range(N)]).astype(np.int32)
+    logp = np.full((N, K), -np.inf)
+    logp[1, 2] = 0.0   # row 1: one-hot on idx[1, 2]; row 0 and the others: empty
+    logp[3, 0] = 0.0
+    loss, lse, rl = orc.forward(H, W, idx, logp)
+    dH, dW = orc.backward(H, W, idx, logp)
+    z = H @ W.T
+    lq = scipy.special.log_softmax(z, axis=1)
+    for n in (0, 2, 4, 5):
+        assert rl[n] == 0.0 and np.all(dH[n] == 0.0)
+    for n, k in ((1, 2), (3, 0)):
+        assert rl[n] == pytest.approx(-lq[n, idx[n, k]], rel=1e-12)
+        G = np.exp(lq[n])
+        G[idx[n, k]] -= 1.0
+        np.testing.assert_allclose(dH[n], G @ W, rtol=1e-10, atol=1e-12)
+    assert loss == pytest.approx(rl.sum(), rel=1e-12)
+    G_all = np.zeros((N, V))
+    for n, k in ((1, 2), (3, 0)):
+        G_all[n] = np.exp(lq[n])
+        G_all[n, idx[n, k]] -= 1.0
+    np.testing.assert_allclose(dW, G_all.T @ H, rtol=1e-10, atol=1e-12)

@@ -103,6 +103,27 @@ def test_repeated_ids_and_empty_slots(fckl):
     assert_parity(got, x, 64)
 
 
+def test_empty_and_one_hot_teacher_rows(fckl):
+    """Positions whose slots are all empty (S = 0: no loss, G = 0, so their dH rows are exactly
+    zero) and positions whose mass sits on one token (S = 1), through both paths."""
+    N, d, V, K, chunk = 300, 128, 3000, 12, 128
+    x = synthetic.make_inputs(N, d, V, K, dtype="bf16", seed=9)
+    empty = np.arange(0, N, 5)
+    onehot = np.setdiff1d(np.arange(2, N, 7), empty)
+    x["logp"][empty, :] = -np.inf
+    x["logp"][onehot, :] = -np.inf
+    x["logp"][onehot, 0] = 0.0
+    got = run_gpu(fckl, x, chunk, "bf16")
+    assert_parity(got, x, chunk)
+    assert np.all(got[2][empty] == 0.0) and np.all(got[3][empty] == 0.0)
+    H, W, idx, logp = to_dev(x, "bf16")
+    loss, lse, rl, dH, dW = fckl.forward_backward(H, W, idx, logp, chunk, row_loss=True)
+    assert fckl.check() == fckl.OK
+    assert float(loss.item()) == got[0]
+    assert np.array_equal(dH.float().cpu().numpy().astype(np.float64), got[3])
+    assert np.array_equal(dW.cpu().numpy().astype(np.float64), got[4])
+
+
 def test_bad_teacher_id_reported(fckl):
     x = synthetic.make_inputs(40, 64, 512, 8, dtype="bf16", seed=8)
     x["idx"][3, 2] = 512
