@@ -103,12 +103,18 @@ def oracle_sample_size(w, target_s=15.0):
 
 
 def calibrated_sample_size(w, seed, target_s):
-    """Rows of an oracle sample taking about target_s seconds on this host: a short timed run
-    of the oracle itself sets the rate (cost is linear in rows)."""
-    n0 = max(8, min(w.N, oracle_sample_size(w, target_s=1.0)))
-    x, W = cpu_inputs(w, seed, n0)
-    t0 = sample_rows_oracle(w, x, W, n0)
-    return max(8, min(w.N, int(n0 * target_s / max(t0, 1e-3))))
+    """Rows of an oracle sample taking about target_s seconds on this host. A call costs a
+    fixed part (e.g. converting W) plus a part linear in rows; two short timed runs of the
+    oracle itself, at n0 and 2 n0 rows, separate the two."""
+    n0 = max(8, min(w.N // 2, oracle_sample_size(w, target_s=1.0)))
+    x, W = cpu_inputs(w, seed, 2 * n0)
+    t1 = sample_rows_oracle(w, x, W, n0)
+    t2 = sample_rows_oracle(w, x, W, 2 * n0)
+    naive = 2 * n0 * target_s / max(t2, 1e-3)  # as if the whole cost grew with rows
+    per_row = (t2 - t1) / n0
+    est = (target_s - max(t1 - per_row * n0, 0.0)) / per_row if per_row > 0 else 4 * naive
+    # timing noise can make the slope look tiny: never more than 4x the plain rate's answer
+    return max(8, min(w.N, int(min(max(est, naive), 4 * naive))))
 
 
 def cpu_baseline(w, seed):
@@ -117,7 +123,7 @@ def cpu_baseline(w, seed):
     t = sample_rows_oracle(w, x, W, n)
     return {"value": n / t, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
             "sample": f"fp64 oracle forward+backward on the first {n} of {w.N} positions "
-                      f"(full V={w.V}, d={w.d}, K={w.K}), {t:.1f} s; cost is linear in positions"}
+                      f"(full V={w.V}, d={w.d}, K={w.K}), {t:.1f} s (sized by two short calibration runs to about 15 s)"}
 
 
 def run_reference(args):
