@@ -91,6 +91,7 @@ def assert_oracle(kept, x, chunk, grad_scale=1.0, weight=None):
     (260, 128, 20000, 100, 260),   # three column segments of the G kernel per position
     (100, 64, 2048, 1024, 64),     # K = 1024: a cache slot in most groups of 8 columns
     (1, 64, 300, 5, 1),            # one position, one-row chunk
+    (40, 8, 16, 16, 16),           # smallest d, V below one tile and one 16-column step, K = V
 ])
 def test_kept_logits_bf16(fckl, N, d, V, K, chunk):
     x = synthetic.make_inputs(N, d, V, K, dtype="bf16", seed=N + V)
