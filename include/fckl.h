@@ -87,7 +87,9 @@ int fckl_forward(const void* H, const void* W, int dtype,
                  void* ws, size_t ws_bytes, void* stream);
 
 /* Backward pass: recomputes every chunk's logits and forms G from `lse` (as written by
- * fckl_forward for the same H, W).
+ * fckl_forward for the same H, W): per logit z with 256-column tile maximum m,
+ * G = weight_n * grad_scale * (S_n exp(m - lse_n) e - p at the cached ids), e = exp(z - m)
+ * rounded to fp16 (relative 2^-11), G rounded to bf16 (2^-9).
  *   grad_scale : upstream derivative d(objective)/d(loss); multiplies dH and dW
  *   dH         : device [N, d] of type `dtype`, overwritten
  *   dW         : device fp32 [V, d], overwritten
