@@ -572,7 +572,7 @@ int chunk_backward(Run& r, int64_t r0, int rows, const void* Hc, bool keep = fal
                      uint64_t(d) * 4, 32, 32)))
     return st;
   const int kbps = static_cast<int>(cdiv(kb_v, splits));
-  ph.sch = {mbr, nbd, kb_v, splits, kbps, 0};
+  ph.sch = {mbr, nbd, kb_v, splits, kbps, 1};
   ph.num_units = mbr * nbd * splits;
   ph.status = r.status;
   ph.c_split_rows = pl.rows_alloc;
