@@ -15,9 +15,9 @@ probable token ids and their values (kept WITHOUT renormalisation) and the
 student's softmax over the whole vocabulary. The student's logits come from
 projecting the hidden states through the output matrix, one chunk of positions
 at a time; the backward pass recomputes each chunk's logits. The pages state
-that the dense, the forward-chunked and the fused variants compute the same
-loss ("数学上完全等价" in the same page; "todas matematicamente equivalentes"
-in "Knowledge distillation barata ... (vazinovacao.com.br)", section "Duas
+that the dense, the forward-chunked and the fused variants give the same loss
+up to rounding (the first page above, section "Fused, chunked KL loss";
+"Knowledge distillation barata ... (vazinovacao.com.br)", section "Duas
 Inovações que Mudam o Jogo"), so the oracle writes out the plain definition.
 
 Notation (per position n, vocabulary entry v, cache slot k):
