@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--recompute", action="store_true",
                     help="--topk: project each chunk twice instead of keeping its logits from pass 1")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cublas", action="store_true",
+                    help="skip the same-shape cuBLAS GEMMs timed (after the timed region) for context")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -273,6 +275,58 @@ def max_over_ranks(value, device=None):
     return float(t.item())
 
 
+def cublas_context(w, dev, H, W_dev, idx, logp, reps=5):
+    """cuBLAS bf16 GEMMs (torch.matmul) of the three per-chunk product shapes, for context
+    beside the fused kernels: the same FLOPs without the epilogues. Timed with CUDA events,
+    median of `reps` after one warm-up; TFLOP/s per shape. The library's own products are
+    timed the same way (short isolated bursts: one chunk's fckl_forward_backward, per-kernel
+    events, median of `reps`), so the two sets compare at the same clock conditions."""
+    import torch
+    import chunked_kl_loss_gb300 as fckl
+    c = min(w.chunk, w.N)
+    g = torch.Generator(device=dev).manual_seed(1)
+    Hc = torch.randn(c, w.d, device=dev, generator=g).to(torch.bfloat16)
+    W = torch.randn(w.V, w.d, device=dev, generator=g).to(torch.bfloat16)
+    G = torch.randn(c, w.V, device=dev, generator=g).to(torch.bfloat16)
+    shapes = {"logits [chunk,d]x[d,V]": lambda: torch.matmul(Hc, W.t()),
+              "dH [chunk,V]x[V,d]": lambda: torch.matmul(G, W),
+              "dW [V,chunk]x[chunk,d]": lambda: torch.matmul(G.t(), Hc)}
+    out = {}
+    for name, fn in shapes.items():
+        fn()
+        times = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+        out[name] = {"ms": ms, "tflops": 2.0 * c * w.d * w.V / (ms / 1e3) / 1e12}
+    del Hc, W, G
+    torch.cuda.empty_cache()
+    # the library's products on one chunk, same timing discipline
+    dt = fckl.BF16 if w.dtype == "bf16" else fckl.F32
+    ws = fckl.Workspace(c, w.d, w.V, w.K, c, dt, dev)
+    Hs, idxs, logps = H[:c], idx[:c], logp[:c]
+    fckl.forward_backward(Hs, W_dev, idxs, logps, c, ws=ws)
+    per = {"fwd_logits_keep": [], "bwd_dH_gemm": [], "bwd_dW_gemm": []}
+    for _ in range(reps):
+        fckl.profile_enable(True)
+        fckl.profile_read()
+        fckl.forward_backward(Hs, W_dev, idxs, logps, c, ws=ws)
+        prof = fckl.profile_read()
+        fckl.profile_enable(False)
+        for k in per:
+            per[k].append(prof[k][0])
+    fckl.check(ws)
+    out["fused (this library), same bursts"] = {
+        k: {"ms": statistics.median(v), "tflops": 2.0 * c * w.d * w.V / (statistics.median(v) / 1e3) / 1e12}
+        for k, v in per.items()}
+    return out
+
+
 def replica_seed(seed, rank):
     """Each rank runs its own replica of the workload on its own seeded inputs."""
     return seed + 1000 * rank
@@ -349,6 +403,7 @@ def run_ours(args):
     peak_bytes = torch.cuda.max_memory_allocated(dev) - base_alloc
 
     t_max = max_over_ranks(elapsed_ms, dev)
+    cublas = cublas_context(w, dev, H, W, idx, logp) if (rank == 0 and not args.no_cublas) else None
 
     # end to end through the public API from pinned host buffers: every step copies its inputs
     # from pinned host memory and reads its loss back. The copies of step i+1 run on a second
@@ -445,6 +500,7 @@ def run_ours(args):
         "kernel_ms_per_step": kernel_ms,
         "clocks": clk,
         "e2e": e2e,
+        "cublas_context": cublas,
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, args.seed)
