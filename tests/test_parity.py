@@ -326,3 +326,43 @@ def test_one_call_captured_in_a_cuda_graph(fckl):
     for u, v in zip((loss, lse, dH, dW), ref_b):
         assert torch.equal(u, v)
     assert not torch.equal(ref_b[0], ref_a[0])
+
+
+def test_calls_from_two_host_threads(fckl):
+    """Two host threads call the one call at the same time, each on its own stream and
+    workspace (ctypes releases the interpreter lock during the call, so the library's host code
+    runs concurrently): the results are those of sequential calls, bit for bit."""
+    import threading
+    xa = synthetic.make_inputs(300, 256, 3000, 20, dtype="bf16", seed=71)
+    xb = synthetic.make_inputs(200, 128, 2500, 10, dtype="bf16", seed=72)
+    ta, tb = to_dev(xa, "bf16"), to_dev(xb, "bf16")
+    ref_a = fckl.forward_backward(*ta, 128)
+    ref_b = fckl.forward_backward(*tb, 64)
+    torch.cuda.synchronize()
+    results, errors = {}, []
+
+    def worker(name, t, chunk, seq):
+        try:
+            torch.cuda.set_device(0)
+            s = torch.cuda.Stream()
+            ws = fckl.Workspace(t[0].shape[0], t[0].shape[1], t[1].shape[0], t[2].shape[1], chunk, fckl.BF16)
+            outs = []
+            with torch.cuda.stream(s):
+                for _ in range(seq):
+                    outs.append(fckl.forward_backward(*t, chunk, ws=ws, stream=s))
+            s.synchronize()
+            results[name] = outs
+        except Exception as e:  # reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=("a", ta, 128, 4)),
+               threading.Thread(target=worker, args=("b", tb, 64, 4))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for outs, ref in ((results["a"], ref_a), (results["b"], ref_b)):
+        for o in outs:
+            for u, v in zip(o, ref):
+                assert torch.equal(u, v)
