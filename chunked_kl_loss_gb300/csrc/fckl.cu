@@ -650,7 +650,9 @@ struct TopkPlan {
   int thr_rows, thr_stride;  // threshold kernel: positions per block, shared-memory row pitch
   int ldz;  // row pitch (elements) of the kept logits
   size_t off_status, off_pm, off_pl, off_pc, off_lse, off_thr, off_cnt, off_cv, off_cz, off_Hb, off_Wb, total;
-  size_t off_Z, total_keep;  // the chunk's fp32 logits from pass 1, read by the collect step
+  // the chunk's fp32 logits from pass 1, read by the collect step, and per position the list
+  // of tiles whose maximum reaches the threshold
+  size_t off_Z, off_live, off_live_cnt, total_keep;
 };
 
 TopkPlan make_topk_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
@@ -683,6 +685,8 @@ TopkPlan make_topk_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
   p.total = o;
   p.ldz = static_cast<int>(rup(V, 8));
   p.off_Z = take(R * p.ldz * 4);
+  p.off_live = take(R * static_cast<size_t>(p.tiles_v) * 4);
+  p.off_live_cnt = take(R * 4);
   p.total_keep = o;
   return p;
 }
@@ -881,20 +885,21 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
     const int tR = tp.thr_rows, tstride = tp.thr_stride;
     const int tblocks = static_cast<int>(cdiv(rows, tR));
     const size_t tsmem = static_cast<size_t>(tR) * tstride * 4;
+    int* live = keep ? reinterpret_cast<int*>(w + tp.off_live) : nullptr;
+    int* live_cnt = keep ? reinterpret_cast<int*>(w + tp.off_live_cnt) : nullptr;
     if ((st = launch(KIND_TOPK_THRESHOLD, s, "topk_threshold", [&] {
            topk_threshold_kernel<<<tblocks, 256, tsmem, s>>>(pm, pl, ld, tiles, rows, tR, tstride, K, lse, thr,
-                                                             cnt);
+                                                             cnt, live, live_cnt);
          })))
       return st;
     // pass 2: every logit at or above the threshold becomes a candidate (logits kept from
     // pass 1, or recomputed)
     const int cmax = tp.cmax;
     if (keep) {
-      const int64_t units = int64_t(rows) * cdiv(V, GRAD_SEG);
-      const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(units, int64_t(di->sms) * 8)));
+      const int grid = std::max(1, std::min(rows, di->sms * 8));
       const int64_t ldz = tp.ldz;
       st = launch(KIND_TOPK_COLLECT_KEPT, s, "topk_collect_from_logits", [&] {
-        topk_collect_kernel<<<grid, GRAD_THREADS, 0, s>>>(Z, ldz, rows, V, thr, cnt, cv, cz, cmax);
+        topk_collect_kernel<<<grid, 256, 0, s>>>(Z, ldz, rows, V, tiles, thr, live, live_cnt, cnt, cv, cz, cmax);
       });
     } else {
       p.thr = thr;

@@ -135,7 +135,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 // is >= thr_n and every top-K entry is at or above it. Also clears the candidate counters.
 // Phase 1 reads the statistics coalesced across the block's rows (lane = row) and stages the
 // maxima, as order-preserving integer keys, in shared memory [R][stride]; phase 2 runs a
-// bitwise search for the K-th largest key, one warp per row.
+// bitwise search for the K-th largest key, one warp per row. With `live` non-null the warp then
+// lists, in tile order, the tiles whose maximum reaches the threshold (live[row][j], j <
+// live_cnt[row]): only those can hold a candidate.
 __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -148,7 +150,8 @@ __global__ void __launch_bounds__(256) topk_threshold_kernel(const float* __rest
                                                              const float* __restrict__ pl, int ld, int tiles,
                                                              int rows, int R, int stride, int K,
                                                              float* __restrict__ lse_out,
-                                                             float* __restrict__ thr_out, int* __restrict__ cnt) {
+                                                             float* __restrict__ thr_out, int* __restrict__ cnt,
+                                                             int* __restrict__ live, int* __restrict__ live_cnt) {
   extern __shared__ uint32_t keys[];  // [R][stride]
   __shared__ float sm[8][32], sl[8][32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -208,61 +211,84 @@ __global__ void __launch_bounds__(256) topk_threshold_kernel(const float* __rest
       thr = order_key_inv(prefix);
     }
     if (lane == 0) thr_out[row2] = thr;
+    if (live) {  // tiles whose maximum is >= thr, i.e. whose key is >= prefix (all when thr = -inf)
+      const uint32_t* kr = keys + r * stride;
+      // keys order -0 below +0 but the comparison with the threshold does not: at a zero
+      // threshold both zeros count
+      const uint32_t kmin = K > tiles ? 0u : (thr == 0.f ? order_key(-0.f) : order_key(thr));
+      int* lr = live + static_cast<int64_t>(row2) * tiles;
+      int base = 0;
+      for (int t0 = 0; t0 < tiles; t0 += 32) {
+        const int t = t0 + lane;
+        const bool on = t < tiles && kr[t] >= kmin;
+        const uint32_t b = __ballot_sync(0xffffffffu, on);
+        if (on) lr[base + __popc(b & ((1u << lane) - 1u))] = t;
+        base += __popc(b);
+      }
+      if (lane == 0) live_cnt[row2] = base;
+    }
   }
 }
 
 // Teacher cache builder, candidate collection from the logits pass 1 kept (fp32 Z, row pitch
 // ld): every logit at or above the position's threshold is appended, with its token id, to
-// the position's candidate list. The same values are compared with the same threshold as in
-// the recomputing collect epilogue, so the candidate set is the same (the append order is
-// not fixed in either; the select step orders the candidates fully). HBM-bound (4 bytes per
-// element); units of one position and GRAD_SEG columns, 8 adjacent columns per thread and
-// step, all of a thread's loads issued before its compares.
-__global__ void __launch_bounds__(GRAD_THREADS) topk_collect_kernel(
-    const float* __restrict__ Z, int64_t ld, int rows, int V, const float* __restrict__ thr,
-    int* __restrict__ cnt, int* __restrict__ cand_v, float* __restrict__ cand_z, int cmax) {
-  const int segs = (V + GRAD_SEG - 1) / GRAD_SEG;
-  const int64_t units = static_cast<int64_t>(rows) * segs;
-  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-    const int row = static_cast<int>(u / segs);
-    const int seg = static_cast<int>(u - static_cast<int64_t>(row) * segs);
-    const float* zr = Z + static_cast<int64_t>(row) * ld;
-    const int c0 = seg * GRAD_SEG + 8 * static_cast<int>(threadIdx.x);
-    // all loads of the unit first (up to 2 * GRAD_STEPS 16-byte loads in flight per thread)
-    float4 z[2 * GRAD_STEPS];
-#pragma unroll
-    for (int i = 0; i < GRAD_STEPS; ++i) {
-      const int c = c0 + i * GRAD_THREADS * 8;
-      if (c + 8 <= V) {
-        z[2 * i] = __ldcs(reinterpret_cast<const float4*>(zr + c));
-        z[2 * i + 1] = __ldcs(reinterpret_cast<const float4*>(zr + c + 4));
-      } else {
-        float x[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) x[t] = c + t < V ? zr[c + t] : -INFINITY;
-        z[2 * i] = make_float4(x[0], x[1], x[2], x[3]);
-        z[2 * i + 1] = make_float4(x[4], x[5], x[6], x[7]);
-      }
-    }
+// the position's candidate list. Only the tiles the threshold kernel listed as live (tile
+// maximum >= threshold; about K of a row's tiles) are read: a tile below it holds no
+// candidate. The same values are compared with the same threshold as in the recomputing
+// collect epilogue, so the candidate set is the same (the append order is not fixed in either;
+// the select step orders the candidates fully). One warp per live tile (a lane takes 8 adjacent
+// columns), each warp loading KC_BATCH tiles before comparing; the block's 8 warps share a
+// position and blocks stride over positions.
+constexpr int KC_BATCH = 4;
+
+__global__ void __launch_bounds__(256) topk_collect_kernel(
+    const float* __restrict__ Z, int64_t ld, int rows, int V, int tiles, const float* __restrict__ thr,
+    const int* __restrict__ live, const int* __restrict__ live_cnt, int* __restrict__ cnt,
+    int* __restrict__ cand_v, float* __restrict__ cand_z, int cmax) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
     const float th = __ldg(thr + row);
+    const int n = __ldg(live_cnt + row);
+    const int* lr = live + static_cast<int64_t>(row) * tiles;
+    const float* zr = Z + static_cast<int64_t>(row) * ld;
+    for (int j0 = w * KC_BATCH; j0 < n; j0 += 8 * KC_BATCH) {
+      float4 z[KC_BATCH][2];
+      int cb[KC_BATCH];
 #pragma unroll
-    for (int i = 0; i < GRAD_STEPS; ++i) {
-      const int c = c0 + i * GRAD_THREADS * 8;
-      const float x[8] = {z[2 * i].x, z[2 * i].y, z[2 * i].z, z[2 * i].w,
-                          z[2 * i + 1].x, z[2 * i + 1].y, z[2 * i + 1].z, z[2 * i + 1].w};
-      uint32_t hits = 0;
+      for (int b = 0; b < KC_BATCH; ++b) {
+        const int j = j0 + b;
+        cb[b] = j < n ? __ldg(lr + j) * VOCAB_TILE + 8 * lane : V;
+        const int c = cb[b];
+        if (c + 8 <= V) {
+          z[b][0] = __ldcs(reinterpret_cast<const float4*>(zr + c));
+          z[b][1] = __ldcs(reinterpret_cast<const float4*>(zr + c + 4));
+        } else {
+          float x[8];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) hits |= (x[t] >= th && c + t < V) ? (1u << t) : 0u;
-      while (hits) {
-        const int t = __ffs(hits) - 1;
-        hits &= hits - 1;
-        const int pos = atomicAdd(cnt + row, 1);
-        if (pos < cmax) {
-          float v = x[0];
+          for (int t = 0; t < 8; ++t) x[t] = c + t < V ? zr[c + t] : -INFINITY;
+          z[b][0] = make_float4(x[0], x[1], x[2], x[3]);
+          z[b][1] = make_float4(x[4], x[5], x[6], x[7]);
+        }
+      }
 #pragma unroll
-          for (int q = 1; q < 8; ++q) v = (q == t) ? x[q] : v;
-          cand_v[static_cast<int64_t>(row) * cmax + pos] = c + t;
-          cand_z[static_cast<int64_t>(row) * cmax + pos] = v;
+      for (int b = 0; b < KC_BATCH; ++b) {
+        const int c = cb[b];
+        const float x[8] = {z[b][0].x, z[b][0].y, z[b][0].z, z[b][0].w,
+                            z[b][1].x, z[b][1].y, z[b][1].z, z[b][1].w};
+        uint32_t hits = 0;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) hits |= (x[t] >= th && c + t < V) ? (1u << t) : 0u;
+        while (hits) {
+          const int t = __ffs(hits) - 1;
+          hits &= hits - 1;
+          const int pos = atomicAdd(cnt + row, 1);
+          if (pos < cmax) {
+            float v = x[0];
+#pragma unroll
+            for (int q = 1; q < 8; ++q) v = (q == t) ? x[q] : v;
+            cand_v[static_cast<int64_t>(row) * cmax + pos] = c + t;
+            cand_z[static_cast<int64_t>(row) * cmax + pos] = v;
+          }
         }
       }
     }

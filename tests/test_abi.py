@@ -55,13 +55,16 @@ def test_workspace_size_rules(fckl):
     assert ws(32768, 3072, 128256, 100, 1024, fckl.BF16) < a
     # fp32 inputs need room for their bf16 copies
     assert ws(64, 256, 4096, 16, 16, fckl.F32) > ws(64, 256, 4096, 16, 16, fckl.BF16)
-    # the top-K builder's kept logits: the same slab on top of its minimum workspace
+    # the top-K builder's kept logits: one chunk of fp32 logits (rows padded to 256, columns to
+    # a multiple of 8) and per position the list of live vocabulary tiles and its length, on top
+    # of its minimum workspace (1 KiB rounding each)
     lib = fckl.load()
     for N, d, V, K, chunk in [(32768, 3072, 128256, 100, 2048), (130, 320, 2057, 100, 200)]:
         extra = (lib.fckl_topk_kept_logits_workspace_bytes(N, d, V, K, chunk, fckl.BF16)
                  - lib.fckl_topk_workspace_bytes(N, d, V, K, chunk, fckl.BF16))
         rows = -(-min(chunk, N) // 256) * 256
-        assert 0 <= extra - rows * (-(-V // 8) * 8) * 4 < 1024
+        tiles = -(-V // 256)
+        assert 0 <= extra - rows * (-(-V // 8) * 8) * 4 - rows * tiles * 4 - rows * 4 < 3072
     # outside the limits: 0
     assert ws(0, 256, 4096, 16, 16, fckl.BF16) == 0
     assert ws(64, 250, 4096, 16, 16, fckl.BF16) == 0  # d % 8 != 0
