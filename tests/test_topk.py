@@ -178,3 +178,23 @@ def test_topk_candidate_overflow_is_reported(fckl, keep):
     Wt2 = synthetic.round_bf16(rng2.standard_normal((V, d), dtype=np.float32) / 4)
     i2, l2 = run_topk(fckl, Ht2, Wt2, K, 64)
     assert_topk_parity(i2, l2, Ht2, Wt2, K)
+
+
+def test_topk_zero_logits(fckl):
+    """All-zero teacher hidden states: every logit is zero, the threshold is zero, and every
+    tile is live. Both pass-2 paths return tokens 0..K-1 (equal logits: smaller id first) with
+    log-probability -log V, bit for bit alike."""
+    N, d, V, K = 40, 64, 1000, 10
+    rng = np.random.default_rng(27)
+    Wt = synthetic.round_bf16(rng.standard_normal((V, d), dtype=np.float32))
+    dev = torch.device("cuda")
+    H = torch.zeros(N, d, dtype=torch.bfloat16, device=dev)
+    W = torch.from_numpy(Wt).to(dev).to(torch.bfloat16)
+    out = {}
+    for keep in (True, False):
+        out[keep] = fckl.teacher_topk(H, W, K, 16, keep_logits=keep)
+        assert fckl.check() == fckl.OK
+    assert torch.equal(out[True][0], out[False][0]) and torch.equal(out[True][1], out[False][1])
+    idx, logp = (t.cpu().numpy() for t in out[True])
+    assert np.array_equal(idx, np.tile(np.arange(K, dtype=np.int32), (N, 1)))
+    assert np.abs(logp + np.log(V)).max() <= 1e-5
