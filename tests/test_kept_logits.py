@@ -92,6 +92,8 @@ def assert_oracle(kept, x, chunk, grad_scale=1.0, weight=None):
     (100, 64, 2048, 1024, 64),     # K = 1024: a cache slot in most groups of 8 columns
     (1, 64, 300, 5, 1),            # one position, one-row chunk
     (40, 8, 16, 16, 16),           # smallest d, V below one tile and one 16-column step, K = V
+    (33, 64, 8, 8, 16),            # V = K = 8: the whole vocabulary cached
+    (64, 8192, 2048, 16, 64),      # wide d: 128 K-blocks per logits tile, 32 N-tiles in dH and dW
 ])
 def test_kept_logits_bf16(fckl, N, d, V, K, chunk):
     x = synthetic.make_inputs(N, d, V, K, dtype="bf16", seed=N + V)
@@ -159,3 +161,18 @@ def test_one_call_needs_no_workspace_beyond_the_slab(fckl):
     with pytest.raises(fckl.FcklError):
         fckl.forward_backward(H, W, idx, logp, 64, ws=Short())
     assert fckl.launch_count() == n0
+
+
+def test_one_token_vocabulary(fckl):
+    """V = K = 1: the softmax is 1, S = p, so the loss is sum_n p_n logp_n and G vanishes. On the
+    device exp(m - lse) is 1 only to within its rounding (~1e-7), so the gradients are bounded
+    absolutely rather than relative to an all-zero reference; the two paths still agree bit for
+    bit."""
+    x = synthetic.make_inputs(8, 64, 1, 1, dtype="bf16", seed=9)
+    kept, rec = run_both(fckl, x, 8, "bf16")
+    assert_bitwise(kept, rec)
+    loss, lse, rl, dH, dW = kept
+    r_loss, r_lse, r_rl = orc.forward(x["H"], x["W"], x["idx"], x["logp"], 8)
+    assert abs(float(loss.item()) - r_loss) <= LOSS_RTOL * abs(r_loss)
+    assert np.abs(lse.cpu().numpy() - r_lse).max() <= 1e-3 * (1 + np.abs(r_lse).max())
+    assert dH.float().abs().max().item() <= 1e-5 and dW.abs().max().item() <= 1e-5
