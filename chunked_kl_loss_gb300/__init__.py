@@ -7,9 +7,11 @@ no CPU fallback: if the library is missing, ``load()`` raises.
 Typical use (tensors on the current CUDA device)::
 
     import chunked_kl_loss_gb300 as fckl
-    loss, lse = fckl.forward(H, W, idx, logp, chunk=2048)
-    dH, dW = fckl.backward(H, W, idx, logp, lse, chunk=2048)
+    loss, lse, dH, dW = fckl.forward_backward(H, W, idx, logp, chunk=2048)   # one call
     fckl.check()            # raises on a device-detected error (bad teacher id, timeout)
+    loss, lse = fckl.forward(H, W, idx, logp, chunk=2048)                    # or separately:
+    dH, dW = fckl.backward(H, W, idx, logp, lse, chunk=2048)                 # recomputes the logits
+    loss = fckl.fused_chunked_kl(H, W, idx, logp, 2048); loss.backward()     # autograd
 
 ``H [N, d]`` and ``W [V, d]`` are bf16 or fp32, ``idx [N, K]`` int32 teacher token ids,
 ``logp [N, K]`` fp32 teacher log-probabilities (not renormalised). The loss is a sum over
