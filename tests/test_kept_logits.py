@@ -102,15 +102,20 @@ def test_kept_logits_bf16(fckl, N, d, V, K, chunk):
     assert_oracle(kept, x, chunk)
 
 
-def test_kept_logits_fp32_inputs(fckl):
+@pytest.mark.parametrize("weighted", [False, True])
+def test_kept_logits_fp32_inputs(fckl, weighted):
     w = synthetic.WORKLOADS["tiny_n64_d256_v4096"]
     x = synthetic.make_inputs(w.N, w.d, w.V, w.K, dtype="f32", seed=41)
-    kept, rec = run_both(fckl, x, w.chunk, "f32", grad_scale=0.25)
+    wt = None
+    if weighted:
+        wt = np.linspace(0.0, 2.0, w.N).astype(np.float32)
+        wt[::9] = 0.0
+    kept, rec = run_both(fckl, x, w.chunk, "f32", grad_scale=0.25, weight=wt)
     assert_bitwise(kept, rec)
     xb = dict(x)
     xb["H"] = synthetic.round_bf16(x["H"])
     xb["W"] = synthetic.round_bf16(x["W"])
-    assert_oracle(kept, xb, w.chunk, grad_scale=0.25)
+    assert_oracle(kept, xb, w.chunk, grad_scale=0.25, weight=wt)
 
 
 def test_kept_logits_weights_repeats_and_empty_slots(fckl):
