@@ -386,9 +386,10 @@ __global__ void __launch_bounds__(256) dh_reduce_kernel(const float* __restrict_
 // recomputing path forms. HBM-bound (4 bytes per element: 2 read, 2 written); a unit is one
 // position and KG_SEG columns, each thread takes 16 adjacent columns per step (two 16-byte
 // loads and stores at the same addresses), GRAD_STEPS steps 4096 columns apart, all loads
-// issued before the arithmetic (128 bytes in flight per thread). The row's ordered cache slots
-// sit in shared memory and each thread walks them with one cursor. Row pitch ld is a multiple
-// of 8 elements; columns in [V, ld) are written as 0.
+// issued before the arithmetic (128 bytes in flight per thread), together with the steps' tile
+// maxima and the row's scalars. The row's ordered cache slots sit in shared memory (two
+// buffers, alternating by unit, so one barrier per unit suffices) and each thread walks them
+// with one cursor. Row pitch ld is a multiple of 8 elements; columns in [V, ld) are written as 0.
 constexpr int KG_COLS = 16;
 constexpr int KG_SEG = GRAD_THREADS * KG_COLS * GRAD_STEPS;
 
@@ -396,36 +397,43 @@ __global__ void __launch_bounds__(GRAD_THREADS) logit_grad_kernel(
     __nv_bfloat16* __restrict__ G, int64_t ld, int rows, int V, int K, const int* __restrict__ sidx,
     const float* __restrict__ sp, const float* __restrict__ S, const float* __restrict__ lse,
     const float* __restrict__ wrow, float gscale, const float* __restrict__ pm, int ld_part) {
-  __shared__ int s_ids[K_LIMIT];
-  __shared__ float s_p[K_LIMIT];
+  __shared__ int s_ids[2][K_LIMIT];  // two units' slots: one barrier per unit suffices
+  __shared__ float s_p[2][K_LIMIT];
   const int segs = (V + KG_SEG - 1) / KG_SEG;
   const int64_t units = static_cast<int64_t>(rows) * segs;
-  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+  int par = 0;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x, par ^= 1) {
     const int row = static_cast<int>(u / segs);
     const int seg = static_cast<int>(u - static_cast<int64_t>(row) * segs);
     __nv_bfloat16* gr = G + static_cast<int64_t>(row) * ld;
     const int c0 = seg * KG_SEG + KG_COLS * static_cast<int>(threadIdx.x);
+    // everything the unit reads is requested first: e, the tile maxima, the row's scalars
     uint4 e[2 * GRAD_STEPS];
+    float mt[GRAD_STEPS];
 #pragma unroll
     for (int i = 0; i < GRAD_STEPS; ++i) {
       const int c = c0 + i * GRAD_THREADS * KG_COLS;
       // 8-column halves wholly past V are not read (the row pitch ends at a multiple of 8)
       e[2 * i] = c < V ? *reinterpret_cast<const uint4*>(gr + c) : make_uint4(0u, 0u, 0u, 0u);
       e[2 * i + 1] = c + 8 < V ? *reinterpret_cast<const uint4*>(gr + c + 8) : make_uint4(0u, 0u, 0u, 0u);
+      mt[i] = c < V ? __ldg(pm + static_cast<int64_t>(c / VOCAB_TILE) * ld_part + row) : 0.f;
     }
-    __syncthreads();  // every thread is done with the previous unit's slots
+    const float wv = wrow ? __ldg(wrow + row) : 1.f;
+    const float sv = __ldg(S + row), lv = __ldg(lse + row);
+    int* ids = s_ids[par];
+    float* pv = s_p[par];
     for (int k = threadIdx.x; k < K; k += GRAD_THREADS) {
-      s_ids[k] = __ldg(sidx + static_cast<int64_t>(row) * K + k);
-      s_p[k] = __ldg(sp + static_cast<int64_t>(row) * K + k);
+      ids[k] = __ldg(sidx + static_cast<int64_t>(row) * K + k);
+      pv[k] = __ldg(sp + static_cast<int64_t>(row) * K + k);
     }
     __syncthreads();
-    const float gs = __fmul_rn(gscale, wrow ? __ldg(wrow + row) : 1.f);
-    const float a = __fmul_rn(gs, __ldg(S + row));
-    const float nl = __fmul_rn(-__ldg(lse + row), LOG2E);
+    const float gs = __fmul_rn(gscale, wv);
+    const float a = __fmul_rn(gs, sv);
+    const float nl = __fmul_rn(-lv, LOG2E);
     int lo = 0, hi = K;  // cursor: first slot whose id is >= c0
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
-      if (s_ids[mid] < c0)
+      if (ids[mid] < c0)
         lo = mid + 1;
       else
         hi = mid;
@@ -435,15 +443,15 @@ __global__ void __launch_bounds__(GRAD_THREADS) logit_grad_kernel(
     for (int i = 0; i < GRAD_STEPS; ++i) {
       const int c = c0 + i * GRAD_THREADS * KG_COLS;
       if (c >= V) break;
-      const float f = tile_factor(a, __ldg(pm + static_cast<int64_t>(c / VOCAB_TILE) * ld_part + row), nl);
+      const float f = tile_factor(a, mt[i], nl);
       const __half* eh = reinterpret_cast<const __half*>(&e[2 * i]);
       float x[KG_COLS];
 #pragma unroll
       for (int t = 0; t < KG_COLS; ++t) x[t] = grad_dense(f, eh[t]);
-      while (k < K && s_ids[k] < c) ++k;
-      while (k < K && s_ids[k] < c + KG_COLS) {
-        const int pos = s_ids[k] - c;
-        const float v = __fmul_rn(gs, s_p[k]);
+      while (k < K && ids[k] < c) ++k;
+      while (k < K && ids[k] < c + KG_COLS) {
+        const int pos = ids[k] - c;
+        const float v = __fmul_rn(gs, pv[k]);
 #pragma unroll
         for (int t = 0; t < KG_COLS; ++t) x[t] = (t == pos) ? __fsub_rn(x[t], v) : x[t];
         ++k;
