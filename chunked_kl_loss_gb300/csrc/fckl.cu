@@ -227,6 +227,10 @@ int check_shape(int64_t N, int d, int V, int K, int chunk, int dt) {
   if (K > V || K > K_LIMIT) return FCKL_ERR_UNSUPPORTED;
   if (d % 8 != 0) return FCKL_ERR_UNSUPPORTED;
   if (N > (int64_t(1) << 40) || V > (1 << 30) || d > (1 << 20)) return FCKL_ERR_UNSUPPORTED;
+  // The rows of one chunk are counted in int (rounded up to 256) and multiply V and d in the
+  // workspace layout; 2^24 rows keeps every product far from overflow (and any workspace of
+  // such a chunk would exceed device memory anyway).
+  if (std::min<int64_t>(chunk, N) > (int64_t(1) << 24)) return FCKL_ERR_UNSUPPORTED;
   return FCKL_OK;
 }
 
@@ -1004,20 +1008,31 @@ namespace {
 
 void* g_static_scratch_addr[64] = {};
 
-// Device address of g_fckl_static_scratch on the current device. The host-side name of the
-// array is only a stand-in, never a device address, so the address is looked up once per
-// device, with that device current, and cached.
-int static_scratch_address(int dev, void** out) {
+// Device address of g_fckl_static_scratch in the current context. The host-side name of the
+// array is only a stand-in, never a device address, so the address is looked up with the
+// device current. Outside stream capture it is looked up again on every call (a table lookup
+// in the runtime), so it stays right after a device reset or under another context of the
+// same device; while `s` is being captured, the address found by the last uncaptured call on
+// this device is used, and a first call on a device made during capture is refused.
+int static_scratch_address(int dev, cudaStream_t s, void** out) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const bool capturing = cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone;
+  cudaGetLastError();  // a refused query must not surface as the next launch's error
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_static_scratch_addr[dev]) {
+  if (!capturing) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_fckl_static_scratch);
     if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
       snprintf(g_last_error, sizeof(g_last_error), "cudaGetSymbolAddress(static scratch): %s",
                cudaGetErrorString(e));
       return FCKL_ERR_CUDA;
     }
     g_static_scratch_addr[dev] = p;
+  } else if (!g_static_scratch_addr[dev]) {
+    snprintf(g_last_error, sizeof(g_last_error),
+             "fckl_forward_static: the first call on a device must come before any stream capture");
+    return FCKL_ERR_CUDA;
   }
   *out = g_static_scratch_addr[dev];
   return FCKL_OK;
@@ -1069,10 +1084,10 @@ extern "C" int fckl_forward_static(const void* H, const void* W, int dtype, cons
   }
   DevInfo* di = nullptr;
   if ((st = device_info(&di))) return st;
-  void* base = nullptr;
-  if ((st = static_scratch_address(di->id, &base))) return st;
-
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* base = nullptr;
+  if ((st = static_scratch_address(di->id, s, &base))) return st;
+
   uint8_t* w = static_cast<uint8_t*>(base);
   unsigned* dstatus = reinterpret_cast<unsigned*>(w + pl.off_status);
   // The array keeps whatever the previous call left; only the status word must start at 0

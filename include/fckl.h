@@ -36,8 +36,9 @@
  *    student"). lse is not weighted.
  *  - `stream` is a cudaStream_t (may be NULL for the legacy default stream). Every call is
  *    asynchronous on it; inputs must stay alive and unmodified until the work completes.
- *  - Limits: N >= 1, 1 <= K <= min(V, 1024), d % 8 == 0 (16-byte rows for the tensor
- *    memory accelerator), chunk >= 1; H, W, dH and dW 16-byte aligned; ws 256-byte aligned.
+ *  - Limits: 1 <= N <= 2^40, 1 <= K <= min(V, 1024), V <= 2^30, d % 8 == 0 (16-byte rows
+ *    for the tensor memory accelerator) and d <= 2^20, 1 <= min(chunk, N) <= 2^24; H, W, dH
+ *    and dW 16-byte aligned; ws 256-byte aligned.
  *  - Return value: FCKL_OK, or an fckl_status naming the first problem found. Argument
  *    errors launch nothing. Errors found on the device (a teacher id outside [0, V), a
  *    pipeline wait that ran out) cannot be returned by an asynchronous call: they are
@@ -70,12 +71,22 @@ typedef enum {
 typedef enum { FCKL_BF16 = 0, FCKL_F32 = 1 } fckl_dtype;
 
 /* Bytes of device workspace that fckl_forward, fckl_backward and fckl_forward_backward need
- * for this shape.
+ * for this shape ("Hugging Face：让知识蒸馏廉价到可大规模运行", paragraph "Fused, chunked KL
+ * loss": only one chunk of positions is ever held, so memory never exceeds one chunk's size;
+ * section "扩展到长上下文": peak memory grows linearly with the sequence length).
  * The size grows with chunk * V (the gradient slab) and with N only through 4 bytes per
- * position; 0 if the shape is outside the limits. */
+ * position; 0 if the shape is outside the limits (including min(chunk, N) above 2^24 rows).
+ * The caller allocates it; the library never does. */
 size_t fckl_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
 
-/* Forward pass.
+/* Forward pass ("Hugging Face：让知识蒸馏廉价到可大规模运行", paragraph "Fused, chunked KL
+ * loss": each chunk's hidden states are projected to logits, folded into the accumulated loss
+ * and dropped before the next chunk; paragraph "离线蒸馏": the loss is taken against the cached
+ * top-100 tokens of every position; "Chunkovaná KL strata ...", section "Čo dopĺňajú
+ * podrobnejšie experimenty": that truncated distribution is not renormalised, S_n < 1).
+ * Per chunk: order the chunk's cache slots by id, then one tensor-core pass over the
+ * vocabulary keeps, per row and 256-column tile, the tile maximum, the sum of exp(z - max) and
+ * the sum of p z at the cached ids; no logit tile leaves the SM.
  *   loss     : device fp32 [1]  <- sum over positions of the per-position KL (a SUM, not a mean)
  *   lse      : device fp32 [N]  <- log-partition of every position, kept for fckl_backward
  *   row_loss : device fp32 [N]  <- per-position KL, or NULL when not wanted
@@ -86,7 +97,11 @@ int fckl_forward(const void* H, const void* W, int dtype,
                  float* loss, float* lse, float* row_loss,
                  void* ws, size_t ws_bytes, void* stream);
 
-/* Backward pass: recomputes every chunk's logits and forms G from `lse` (as written by
+/* Backward pass ("Hugging Face：让知识蒸馏廉价到可大规模运行", paragraph "Fused, chunked KL
+ * loss": the backward pass recomputes each chunk instead of storing it, so the projection runs
+ * twice; the closing paragraph names the closed-form gradient, which is the derivative of the
+ * loss above: G_n = S_n softmax(z_n) - p_sparse_n, dH = G W, dW = G^T H).
+ * Recomputes every chunk's logits and forms G from `lse` (as written by
  * fckl_forward for the same H, W): per logit z with 256-column tile maximum m,
  * G = weight_n * grad_scale * (S_n exp(m - lse_n) e - p at the cached ids), e = exp(z - m)
  * rounded to fp16 (relative 2^-11), G rounded to bf16 (2^-9).
@@ -143,7 +158,10 @@ int fckl_forward_backward(const void* H, const void* W, int dtype,
  * of up to 4096 positions fits.
  *
  * The first call on a device looks up the device address of the array (cudaGetSymbolAddress
- * with that device current) and caches it; make that first call before any stream capture.
+ * with that device current); make that first call before any stream capture. Later calls look
+ * the address up again unless their stream is being captured (then the address of the last
+ * uncaptured call on that device is used), so a device reset or another context of the same
+ * device gets the array's current address.
  * Every call on a device shares the one array, which keeps the previous call's contents (the
  * call clears the status word it needs zeroed): calls whose work overlaps on the GPU (on
  * different streams, or from different threads) race on it and must be serialised by the
@@ -178,18 +196,21 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype,
                       int32_t* idx, float* logp,
                       void* ws, size_t ws_bytes, void* stream);
 
-/* Synchronises `stream`, returns the status found on the device by the last call that
+/* Interface addition, no counterpart on the pages (they describe no device interface).
+ * Synchronises `stream`, returns the status found on the device by the last call that
  * used `ws` (FCKL_OK if none), and clears it. */
 int fckl_check(void* ws, void* stream);
 
-/* Self-test of failure detection: launches one kernel that waits, with the same bounded
+/* Interface addition, no counterpart on the pages.
+ * Self-test of failure detection: launches one kernel that waits, with the same bounded
  * wait the pipeline kernels use but a 50 ms limit, on a barrier nothing arrives at. The wait
  * gives up, the kernel records a timeout in the status word at the start of ws and returns
  * normally, so fckl_check(ws, stream) then returns FCKL_ERR_TIMEOUT and the context stays
  * usable. ws: device buffer of at least 256 bytes (any fckl workspace will do). */
 int fckl_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream);
 
-/* Static text for a status code. */
+/* Diagnostics below: interface additions, no counterpart on the pages.
+ * Static text for a status code. */
 const char* fckl_status_string(int status);
 
 /* Text of the last CUDA error seen by this library in this process ("" if none). */

@@ -72,6 +72,13 @@ def test_workspace_size_rules(fckl):
     assert ws(64, 256, 4096, 1025, 16, fckl.BF16) == 0
     assert ws(64, 256, 4096, 16, 0, fckl.BF16) == 0
     assert ws(64, 256, 4096, 16, 16, 7) == 0
+    # a chunk whose row count (rounded up to 256) no longer fits the int arithmetic of the
+    # layout is refused, also through the no-workspace forward; min(chunk, N) is what counts
+    big = (1 << 24) + 1
+    assert ws(1 << 30, 256, 4096, 16, big, fckl.BF16) == 0
+    assert ws(1 << 30, 256, 4096, 16, 2**31 - 1, fckl.BF16) == 0
+    assert ws(4096, 256, 4096, 16, 2**31 - 1, fckl.BF16) == ws(4096, 256, 4096, 16, 4096, fckl.BF16) > 0
+    assert lib.fckl_topk_workspace_bytes(1 << 30, 256, 4096, 16, big, fckl.BF16) == 0
 
 
 def test_argument_errors_launch_nothing(fckl):
@@ -94,6 +101,9 @@ def test_argument_errors_launch_nothing(fckl):
                              z) == fckl.ERR_WORKSPACE
     assert lib.fckl_forward_backward(p, p, 0, p, p, z, 64, 256, 4096, 16, 16, ctypes.c_float(1.0), p, p, z, p,
                                      p, p, 16, z) == fckl.ERR_WORKSPACE
+    # a chunk above 2^24 rows
+    assert lib.fckl_forward(p, p, 0, p, p, z, 1 << 30, 256, 4096, 16, (1 << 24) + 1, p, p, z, p, 1 << 62,
+                            z) == fckl.ERR_UNSUPPORTED
     assert lib.fckl_selftest_wait_timeout(p, 16, z) == fckl.ERR_ARG
     assert lib.fckl_check(z, z) == fckl.ERR_ARG
     assert lib.fckl_launch_count() == before
