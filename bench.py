@@ -62,6 +62,9 @@ def parse():
     ap.add_argument("--no-cublas", action="store_true",
                     help="skip the same-shape cuBLAS GEMMs timed (after the timed region) for context")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-path", action="store_true",
+                    help="time only --api's path (by default the other structure is timed too, over the same "
+                         "steps, and reported as a sub-object of the line)")
     return ap.parse_args()
 
 
@@ -87,14 +90,12 @@ def sample_rows_oracle(w, x_rows, W_full, n_rows):
     return time.perf_counter() - t0
 
 
-def cpu_inputs(w, seed, n_rows):
-    """The first n_rows positions of the workload's inputs, and the full W (same recipe)."""
-    H = synthetic.hidden_states(n_rows, w.d, seed + 0)
-    W = synthetic.output_projection(w.V, w.d, seed + 1)
-    idx, logp = synthetic.teacher_cache(n_rows, w.V, w.K, seed + 2)
-    if w.dtype == "bf16":
-        H, W = synthetic.round_bf16(H), synthetic.round_bf16(W)
-    return {"H": H, "idx": idx, "logp": logp}, W
+def cpu_inputs(w, seed):
+    """The workload's inputs exactly as the device sees them (bf16 values widened to fp32 for
+    bf16 workloads): positions of a CPU sample are sliced from these, so a sample of n
+    positions is the first n positions of the benched workload."""
+    x = synthetic.make_inputs(w.N, w.d, w.V, w.K, dtype=w.dtype, seed=seed)
+    return {"H": x["H"], "idx": x["idx"], "logp": x["logp"]}, x["W"]
 
 
 def oracle_sample_size(w, target_s=15.0):
@@ -104,27 +105,28 @@ def oracle_sample_size(w, target_s=15.0):
     return max(8, min(w.N, guess))
 
 
-def calibrated_sample_size(w, seed, target_s):
+def calibrated_sample_size(w, x, W, target_s):
     """Rows of an oracle sample taking about target_s seconds on this host. A call costs a
     fixed part (e.g. converting W) plus a part linear in rows; two short timed runs of the
-    oracle itself, at n0 and 2 n0 rows, separate the two."""
-    n0 = max(8, min(w.N // 2, oracle_sample_size(w, target_s=1.0)))
-    x, W = cpu_inputs(w, seed, 2 * n0)
+    oracle itself, at n0 and 2 n0 rows, separate the two. Never more rows than ``x`` holds."""
+    n_max = len(x["H"]) if x else w.N
+    n0 = max(8, min(n_max // 2, oracle_sample_size(w, target_s=1.0)))
     t1 = sample_rows_oracle(w, x, W, n0)
     t2 = sample_rows_oracle(w, x, W, 2 * n0)
     naive = 2 * n0 * target_s / max(t2, 1e-3)  # as if the whole cost grew with rows
     per_row = (t2 - t1) / n0
     est = (target_s - max(t1 - per_row * n0, 0.0)) / per_row if per_row > 0 else 4 * naive
     # timing noise can make the slope look tiny: never more than 4x the plain rate's answer
-    return max(8, min(w.N, int(min(max(est, naive), 4 * naive))))
+    return max(8, min(n_max, int(min(max(est, naive), 4 * naive))))
 
 
-def cpu_baseline(w, seed):
-    n = calibrated_sample_size(w, seed, target_s=15.0)
-    x, W = cpu_inputs(w, seed, n)
+def cpu_baseline(w, x, W):
+    """The fp64 oracle, as it stands, timed on the host cores on the first n positions of the
+    benched inputs ``x`` (n sized for about 15 s)."""
+    n = calibrated_sample_size(w, x, W, target_s=15.0)
     t = sample_rows_oracle(w, x, W, n)
     return {"value": n / t, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-            "sample": f"fp64 oracle forward+backward on the first {n} of {w.N} positions "
+            "sample": f"fp64 oracle forward+backward on the first {n} of the {w.N} benched positions "
                       f"(full V={w.V}, d={w.d}, K={w.K}), {t:.1f} s (sized by two short calibration runs to about 15 s)"}
 
 
@@ -134,7 +136,7 @@ def run_reference(args):
         return 0
     w = synthetic.WORKLOADS[args.workload]
     n = max(8, oracle_sample_size(w, target_s=6.0))
-    x, W = cpu_inputs(w, args.seed, n)
+    x, W = cpu_inputs(w, args.seed)
     for _ in range(args.warmup):
         sample_rows_oracle(w, x, W, min(n, 8))
     times = [sample_rows_oracle(w, x, W, n) for _ in range(args.steps)]
@@ -146,8 +148,8 @@ def run_reference(args):
             "data": "synthetic",
             "config": config_of(w, args.api),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-                             "sample": f"each step: fp64 oracle forward+backward on {n} of {w.N} positions "
-                                       f"(full V, d)"},
+                             "sample": f"each step: fp64 oracle forward+backward on the first {n} of the "
+                                       f"{w.N} positions of the workload (full V, d)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -327,6 +329,38 @@ def cublas_context(w, dev, H, W_dev, idx, logp, reps=5):
     return out
 
 
+def path_summary(w, api, t_ms, steps, world, prof, peak_sus, peak_src):
+    """Throughput of one timed path and the roofline of its dominant kernel.
+
+    tflops_8NdV is the metric's count (8 N d V FLOPs per step: the four products of the
+    recomputing structure) over the step time; it is a count, not a roofline fraction, since
+    the one call runs only three of the four products. The roofline fraction is taken on the
+    executed products only (tflops_executed) and, per kernel, on the dominant kernel's own
+    FLOPs over its CUDA-event time."""
+    ms_step = t_ms / steps
+    products = 3 if api == "fused" else 4  # with kept logits the backward's logits product is not run
+    tfl = w.flops() / (ms_step / 1e3) / 1e12
+    tfl_exec = w.flops() * products / 4 / (ms_step / 1e3) / 1e12
+    kname, (kms, kn) = max(prof.items(), key=lambda kv: kv[1][0])
+    roof = None
+    if kname in GEMM_KERNELS and kn > 0:
+        flops_per_launch = 2.0 * w.N * w.d * w.V * steps / kn
+        achieved = flops_per_launch / (kms / kn / 1e3) / 1e12
+        roof = {"kernel": kname, "bound": "tensor", "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
+                "frac": achieved / peak_sus, "traffic": profile_traffic(kname, w.name),
+                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step)",
+                "flops_per_launch": flops_per_launch, "avg_launch_ms": kms / kn}
+    total = max(1e-9, sum(u[0] for u in prof.values()))
+    return {"value": world * w.N * steps / (t_ms / 1e3), "ms_per_step": ms_step,
+            "tflops_8NdV": tfl,
+            "tflops_8NdV_note": ("count: 8NdV FLOPs over the step time; this path executes "
+                                 f"{products} of the 4 products (2NdV each)"),
+            "tflops_executed": tfl_exec, "tflops_executed_frac_of_sustained": tfl_exec / peak_sus,
+            "roofline": roof,
+            "kernel_shares": {k: round(v[0] / total, 4) for k, v in prof.items() if v[1]},
+            "kernel_ms_per_step": sum(v[0] for v in prof.values()) / steps}
+
+
 def replica_seed(seed, rank):
     """Each rank runs its own replica of the workload on its own seeded inputs."""
     return seed + 1000 * rank
@@ -357,14 +391,13 @@ def run_ours(args):
     base_alloc = torch.cuda.memory_allocated(dev)
     H, W, idx, logp = (host[k].to(dev) for k in ("H", "W", "idx", "logp"))
     dt = fckl.BF16 if w.dtype == "bf16" else fckl.F32
-    keep = args.api == "fused"
     ws = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, dt, dev)
     dH = torch.empty_like(H)
     dW = torch.empty(w.V, w.d, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        if args.api == "fused":
+    def step(api):
+        if api == "fused":
             loss, _, _, _ = fckl.forward_backward(H, W, idx, logp, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW)
             return loss
         loss, lse = fckl.forward(H, W, idx, logp, w.chunk, ws=ws, stream=stream)
@@ -377,30 +410,40 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    for _ in range(args.warmup):
-        step()
-    fckl.check(ws)
-    barrier()
+    def timed(api):
+        """W warm-up steps, then exactly K timed steps between barriers, with CUDA events on
+        the launch stream, the library's per-kernel events and the clock sampler."""
+        for _ in range(args.warmup):
+            step(api)
+        fckl.check(ws)
+        barrier()
+        clocks = ClockSampler(local_rank)
+        clocks.start()
+        fckl.profile_enable(True)
+        fckl.profile_read()
+        launches0 = fckl.launch_count()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step(api)
+        e1.record(stream)
+        barrier()
+        elapsed = e0.elapsed_time(e1)
+        n_launch = fckl.launch_count() - launches0
+        prof_ = fckl.profile_read()
+        fckl.profile_enable(False)
+        clk_ = clocks.stop()
+        fckl.check(ws)
+        return elapsed, n_launch, prof_, clk_
 
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    fckl.profile_enable(True)
-    fckl.profile_read()
-    launches0 = fckl.launch_count()
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        loss = step()
-    e1.record(stream)
-    barrier()
-    elapsed_ms = e0.elapsed_time(e1)
-    launches = fckl.launch_count() - launches0
-    prof = fckl.profile_read()
-    fckl.profile_enable(False)
-    clk = clocks.stop()
-    fckl.check(ws)
+    elapsed_ms, launches, prof, clk = timed(args.api)
     peak_bytes = torch.cuda.max_memory_allocated(dev) - base_alloc
+    other = None
+    if not args.no_other_path:  # the other structure over the same steps, same inputs
+        other_api = "separate" if args.api == "fused" else "fused"
+        o_ms, o_launch, o_prof, o_clk = timed(other_api)
+        other = (other_api, max_over_ranks(o_ms, dev), o_launch, o_prof, o_clk)
 
     t_max = max_over_ranks(elapsed_ms, dev)
     cublas = cublas_context(w, dev, H, W, idx, logp) if (rank == 0 and not args.no_cublas) else None
@@ -467,43 +510,37 @@ def run_ours(args):
             dist.destroy_process_group()
         return 0
 
-    ms_step = t_max / args.steps
-    value = world * w.N * args.steps / (t_max / 1e3)
-    tflops = w.flops() / (ms_step / 1e3) / 1e12  # the metric's count: 8NdV, four products
-    products = 3 if keep else 4  # with kept logits the backward's logits product is not run
-    tflops_exec = w.flops() * products / 4 / (ms_step / 1e3) / 1e12
     peaks, peak_src = measured_peaks()
     peak_sus = peak_value(peaks, "bf16_tflops_sustained")
-    # dominant kernel: largest share of the measured launch time
-    kname, (kms, kn) = max(prof.items(), key=lambda kv: kv[1][0])
-    roof = None
-    if kname in GEMM_KERNELS and kn > 0:
-        flops_per_launch = 2.0 * w.N * w.d * w.V * args.steps / kn
-        achieved = flops_per_launch / (kms / kn / 1e3) / 1e12
-        traffic = profile_traffic(kname, w.name)
-        roof = {"kernel": kname, "bound": "tensor", "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
-                "frac": achieved / peak_sus, "traffic": traffic,
-                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step)",
-                "flops_per_launch": flops_per_launch, "avg_launch_ms": kms / kn}
-    shares = {k: round(v[0] / max(1e-9, sum(u[0] for u in prof.values())), 4) for k, v in prof.items() if v[1]}
-    kernel_ms = sum(v[0] for v in prof.values()) / args.steps  # device time of the library's kernels
+    head = path_summary(w, args.api, t_max, args.steps, world, prof, peak_sus, peak_src)
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generators; no dataset)",
         "config": config_of(w, args.api),
-        "tflops": tflops, "tflops_executed": tflops_exec, "tflops_executed_frac_of_peak": tflops_exec / peak_sus,
+        "tflops_8NdV": head["tflops_8NdV"], "tflops_8NdV_note": head["tflops_8NdV_note"],
+        "tflops_executed": head["tflops_executed"],
+        "tflops_executed_frac_of_sustained": head["tflops_executed_frac_of_sustained"],
         "peak_gib": peak_bytes / 2**30,
         "gpu_launches": launches,
-        "roofline": roof,
-        "kernel_shares": shares,
-        "kernel_ms_per_step": kernel_ms,
+        "roofline": head["roofline"],
+        "kernel_shares": head["kernel_shares"],
+        "kernel_ms_per_step": head["kernel_ms_per_step"],
         "clocks": clk,
         "e2e": e2e,
         "cublas_context": cublas,
     }
+    if other is not None:
+        o_api, o_ms, o_launch, o_prof, o_clk = other
+        o = path_summary(w, o_api, o_ms, args.steps, world, o_prof, peak_sus, peak_src)
+        o.update({"api": o_api, "logits": config_of(w, o_api)["logits"], "gpu_launches": o_launch,
+                  "clocks": o_clk, "steps": args.steps, "warmup": args.warmup})
+        line[o_api] = o
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(w, args.seed)
+        n_host = min(w.N, 16384)  # the oracle's sample is far smaller; slice the benched inputs
+        xs = {"H": host["H"][:n_host].float().numpy(), "idx": host["idx"][:n_host].numpy(),
+              "logp": host["logp"][:n_host].numpy()}
+        line["cpu_baseline"] = cpu_baseline(w, xs, host["W"].float().numpy())
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -52,8 +52,7 @@ def test_oracle_sample_is_sized_from_two_calibration_runs(monkeypatch):
         return 2.0 + 0.01 * n
 
     monkeypatch.setattr(bench, "sample_rows_oracle", fake_time)
-    monkeypatch.setattr(bench, "cpu_inputs", lambda w_, seed, n: ({}, None))
-    n = bench.calibrated_sample_size(w, 0, 15.0)
+    n = bench.calibrated_sample_size(w, {}, None, 15.0)
     assert len(calls) == 2 and calls[1] == 2 * calls[0]
     # (15 s - 2 s) / 10 ms = 1300 positions, within the 4x clamp of the plain estimate
     assert abs(n - 1300) <= 2
@@ -61,5 +60,19 @@ def test_oracle_sample_is_sized_from_two_calibration_runs(monkeypatch):
     # noisy timings (the larger run no slower): never more than 4x the plain rate's answer
     monkeypatch.setattr(bench, "sample_rows_oracle", lambda w_, x, W, n: 3.0)
     n0 = bench.oracle_sample_size(w, target_s=1.0)
-    n = bench.calibrated_sample_size(w, 0, 15.0)
+    n = bench.calibrated_sample_size(w, {}, None, 15.0)
     assert n <= 4 * int(2 * n0 * 15.0 / 3.0) + 1
+
+
+def test_cpu_sample_is_the_first_positions_of_the_benched_inputs():
+    """The oracle's CPU sample slices the workload's own inputs: its first n positions are
+    the benched positions 0..n-1, bit for bit (the teacher cache's redraws of rows with a
+    repeated id depend on the row count, so regenerating at n rows would give other rows)."""
+    import numpy as np
+    w = synthetic.WORKLOADS["n8192_d3072_v128256"]
+    x, W = bench.cpu_inputs(w, 0)
+    full = synthetic.make_inputs(w.N, w.d, w.V, w.K, dtype=w.dtype, seed=0)
+    assert x["H"].shape == (w.N, w.d) and W.shape == (w.V, w.d)
+    for k in ("H", "idx", "logp"):
+        assert np.array_equal(x[k][:100], full[k][:100])
+    assert np.array_equal(W, full["W"])
