@@ -246,21 +246,23 @@ def _autograd_function():
     import torch
 
     class FusedChunkedKL(torch.autograd.Function):
-        """Autograd wrapper. When H or W needs a gradient, the forward runs the one call
-        (fckl_forward_backward with grad_scale 1) and holds dH and dW; the backward multiplies
-        them by the upstream gradient on the device (fp32 product, one rounding to H's dtype;
-        no host synchronisation; exact when the upstream gradient is 1). Without gradients the
-        forward runs fckl_forward alone."""
+        """Autograd wrapper of scale * loss. When H or W needs a gradient, the forward runs the
+        one call (fckl_forward_backward with grad_scale = scale) and holds dH and dW; the
+        backward multiplies them by the upstream gradient g on the device (fp32 product, one
+        rounding to H's dtype; no host synchronisation). For g = 1 (``out.backward()`` on the
+        scalar itself) the held gradients are returned as the library wrote them, so a caller
+        that folds its reduction (e.g. scale = 1/N for a mean) into ``scale`` gets dH rounded
+        once. Without gradients the forward runs fckl_forward alone."""
 
         @staticmethod
-        def forward(ctx, H, W, idx, logp, chunk, weight):
+        def forward(ctx, H, W, idx, logp, chunk, weight, scale):
             if ctx.needs_input_grad[0] or ctx.needs_input_grad[1]:
-                loss, _, dH, dW = forward_backward(H, W, idx, logp, chunk, weight=weight)
+                loss, _, dH, dW = forward_backward(H, W, idx, logp, chunk, grad_scale=scale, weight=weight)
                 ctx.grads = (dH, dW)
             else:
                 loss, _ = forward(H, W, idx, logp, chunk, weight=weight)
                 ctx.grads = None
-            return loss[0]
+            return loss[0] if scale == 1.0 else loss[0] * scale
 
         @staticmethod
         def backward(ctx, g):
@@ -269,7 +271,7 @@ def _autograd_function():
             g32 = g.float()
             gH = (dH.float() * g32).to(dH.dtype) if ctx.needs_input_grad[0] else None
             gW = dW * g32 if ctx.needs_input_grad[1] else None
-            return gH, gW, None, None, None, None
+            return gH, gW, None, None, None, None, None
 
     return FusedChunkedKL
 
@@ -277,13 +279,15 @@ def _autograd_function():
 _FusedChunkedKL = None
 
 
-def fused_chunked_kl(H, W, idx, logp, chunk, weight=None):
-    """The loss as a differentiable scalar: gradients reach H and W through autograd (W's
-    fp32 gradient is cast to W's dtype by autograd)."""
+def fused_chunked_kl(H, W, idx, logp, chunk, weight=None, scale=1.0):
+    """``scale`` times the loss as a differentiable scalar: gradients reach H and W through
+    autograd (W's fp32 gradient is cast to W's dtype by autograd). Fold a known reduction into
+    ``scale`` (1/N for a mean over positions) rather than dividing the result: the library then
+    applies it before dH's one rounding."""
     global _FusedChunkedKL
     if _FusedChunkedKL is None:
         _FusedChunkedKL = _autograd_function()
-    return _FusedChunkedKL.apply(H, W, idx, logp, chunk, weight)
+    return _FusedChunkedKL.apply(H, W, idx, logp, chunk, weight, float(scale))
 
 
 def teacher_topk(Ht, Wt, K, chunk, ws=None, stream=None, keep_logits=True):

@@ -239,6 +239,26 @@ def test_autograd_wrapper_paths(fckl):
     assert "fwd_logits_lse" in ran and not ran & {"bwd_dH_gemm", "bwd_dW_gemm", "fwd_logits_keep"}
 
 
+def test_autograd_scale_is_applied_before_the_one_rounding(fckl):
+    """A mean folded into ``scale``: the value is scale * loss and the gradients are the one
+    call's outputs at grad_scale = scale bit for bit (dH rounded once), within the tolerance of
+    the oracle's gradients of the mean."""
+    N, d, V, K, chunk = 200, 128, 2048, 20, 64
+    x = synthetic.make_inputs(N, d, V, K, dtype="bf16", seed=14)
+    H, W, idx, logp = to_dev(x, "bf16")
+    loss_ref, _, dH_ref, dW_ref = fckl.forward_backward(H, W, idx, logp, chunk, grad_scale=1.0 / N)
+    Hg, Wg = H.clone().requires_grad_(True), W.clone().requires_grad_(True)
+    out = fckl.fused_chunked_kl(Hg, Wg, idx, logp, chunk, scale=1.0 / N)
+    out.backward()
+    assert torch.equal(out.detach(), loss_ref[0] * (1.0 / N))
+    assert torch.equal(Hg.grad, dH_ref)
+    assert torch.equal(Wg.grad, dW_ref.to(torch.bfloat16))
+    r_dH, r_dW = orc.backward(x["H"], x["W"], x["idx"], x["logp"], 1.0 / N, chunk)
+    gH = Hg.grad.float().cpu().numpy()
+    assert np.abs(gH - r_dH).max() <= GRAD_TOL * np.abs(r_dH).max()
+    assert np.abs(dW_ref.cpu().numpy() - r_dW).max() <= GRAD_TOL * np.abs(r_dW).max()
+
+
 def test_bounded_wait_times_out_and_context_survives(fckl):
     """Failure detection without a fault: a wait that nothing satisfies gives up, the status
     word says so, and the next call on the same context works."""
