@@ -5,9 +5,11 @@
 One step = one forward + backward over the whole workload (all chunks), inputs resident in
 HBM: one fckl_forward_backward call (--api fused, the default: each chunk's backward forms G
 from what its forward kept in the gradient slab) or fckl_forward then fckl_backward (--api
-separate: the backward recomputes each chunk's logits). Prints one JSON line (rank 0). Under torchrun each rank runs its own
-replica of the workload (the loss has no exchange step on one GPU: replicas only) and
-the whole-job value is the positions of all ranks over the slowest rank's time.
+separate: the backward recomputes each chunk's logits); the other structure is timed too over
+the same steps and reported in a sub-object of the line. Prints one JSON line (rank 0). Under
+torchrun each rank runs its own replica of the workload, or with --dp its own positions of a
+data-parallel step (W replicated, dW and the loss all-reduced every step); the whole-job value
+is the positions of all ranks over the slowest rank's time.
 
 ``--impl reference`` times the fp64 CPU oracle, as it stands, on the host cores, on a
 bounded sample of positions of the same workload (the pages ship no runnable code).
@@ -62,6 +64,9 @@ def parse():
     ap.add_argument("--no-cublas", action="store_true",
                     help="skip the same-shape cuBLAS GEMMs timed (after the timed region) for context")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dp", action="store_true",
+                    help="under torchrun: data-parallel step (each rank its own positions, W replicated, dW and "
+                         "the loss all-reduced inside the timed step) instead of independent replicas")
     ap.add_argument("--no-other-path", action="store_true",
                     help="time only --api's path (by default the other structure is timed too, over the same "
                          "steps, and reported as a sub-object of the line)")
@@ -155,9 +160,11 @@ def run_reference(args):
     return 0
 
 
-def config_of(w, api="fused"):
+def config_of(w, api="fused", dp_world=0):
+    par = (f"dp{dp_world}: {w.N} positions per rank, W replicated, dW and loss all-reduced every step"
+           if dp_world > 1 else "replicas")
     return {"workload": w.name, "N": w.N, "d": w.d, "V": w.V, "K": w.K, "chunk": w.chunk,
-            "input_dtype": w.dtype, "parallelism": "replicas", "api": api,
+            "input_dtype": w.dtype, "parallelism": par, "api": api,
             "logits": ("kept by the forward (fp16 exp(z - tile max) in the gradient slab)" if api == "fused"
                        else "recomputed in the backward"),
             "l2": "inputs larger than L2 (W alone is %.0f MB)" % (w.V * w.d * 2 / 1e6)}
@@ -399,9 +406,11 @@ def run_ours(args):
     def step(api):
         if api == "fused":
             loss, _, _, _ = fckl.forward_backward(H, W, idx, logp, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW)
-            return loss
-        loss, lse = fckl.forward(H, W, idx, logp, w.chunk, ws=ws, stream=stream)
-        fckl.backward(H, W, idx, logp, lse, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW)
+        else:
+            loss, lse = fckl.forward(H, W, idx, logp, w.chunk, ws=ws, stream=stream)
+            fckl.backward(H, W, idx, logp, lse, w.chunk, ws=ws, stream=stream, dH=dH, dW=dW)
+        if args.dp:  # the data-parallel exchange: sum dW and the loss over the ranks
+            fckl.allreduce_loss_and_dW(loss, dW)
         return loss
 
     def barrier():
@@ -517,7 +526,7 @@ def run_ours(args):
         "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generators; no dataset)",
-        "config": config_of(w, args.api),
+        "config": config_of(w, args.api, world if args.dp else 0),
         "tflops_8NdV": head["tflops_8NdV"], "tflops_8NdV_note": head["tflops_8NdV_note"],
         "tflops_executed": head["tflops_executed"],
         "tflops_executed_frac_of_sustained": head["tflops_executed_frac_of_sustained"],

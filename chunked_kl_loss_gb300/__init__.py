@@ -23,7 +23,8 @@ import ctypes
 import os
 
 __all__ = ["LIB_PATH", "FcklError", "load", "workspace_bytes", "Workspace", "forward", "backward",
-           "forward_backward", "fused_chunked_kl", "teacher_topk", "check", "launch_count", "profile_enable", "profile_read",
+           "forward_backward", "fused_chunked_kl", "teacher_topk", "check", "shard_range",
+           "allreduce_loss_and_dW", "data_parallel_forward_backward", "launch_count", "profile_enable", "profile_read",
            "kernel_names", "OK", "ERR_ARG", "ERR_INDEX", "ERR_CUDA", "ERR_TIMEOUT",
            "ERR_WORKSPACE", "ERR_UNSUPPORTED", "ERR_CAPACITY"]
 
@@ -288,6 +289,63 @@ def fused_chunked_kl(H, W, idx, logp, chunk, weight=None, scale=1.0):
     if _FusedChunkedKL is None:
         _FusedChunkedKL = _autograd_function()
     return _FusedChunkedKL.apply(H, W, idx, logp, chunk, weight, float(scale))
+
+
+def shard_range(N: int, rank: int, world: int):
+    """Contiguous positions [start, end) of rank ``rank`` out of ``world`` for a global batch of
+    N positions: the first N % world ranks take one position more. Every position belongs to
+    exactly one rank and the ranks' ranges are in rank order."""
+    if world < 1 or not 0 <= rank < world or N < 0:
+        raise ValueError("need 0 <= rank < world and N >= 0")
+    base, extra = divmod(N, world)
+    start = rank * base + min(rank, extra)
+    return start, start + base + (1 if rank < extra else 0)
+
+
+def allreduce_loss_and_dW(loss, dW, group=None):
+    """Sums the loss [1] and dW [V, d] (fp32) over the ranks of ``group`` in place: the one
+    exchange step of the data-parallel loss (the positions are independent except through
+    dW, whose gradient is a sum over positions, and the loss, a sum too). With the NCCL
+    backend the device tensors are reduced directly; with gloo (CPU ranks, or GPU ranks that
+    exchange through the host) device tensors are staged through host memory."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size(group) == 1:
+        return loss, dW
+    via_host = dW.is_cuda and dist.get_backend(group) != "nccl"
+    for t in (dW, loss):
+        if via_host:
+            h = t.cpu()
+            dist.all_reduce(h, op=dist.ReduceOp.SUM, group=group)
+            t.copy_(h)
+        else:
+            dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+    if via_host:
+        torch.cuda.current_stream(dW.device).synchronize()
+    return loss, dW
+
+
+def data_parallel_forward_backward(H, W, idx, logp, chunk, grad_scale=1.0, ws=None, stream=None, weight=None,
+                                   dH=None, dW=None, group=None):
+    """One data-parallel step: ``H``, ``idx``, ``logp`` (and ``weight``) hold this rank's
+    contiguous range of positions (``shard_range``), ``W`` is replicated. The rank runs the one
+    call on its positions, then the loss and dW are summed over the ranks; lse and dH stay with
+    the rank's positions. Returns (loss of all ranks, lse, dH, dW of all ranks). A rank with no
+    positions contributes zeros to both sums."""
+    if H.shape[0] == 0:
+        import torch
+        loss = torch.zeros(1, dtype=torch.float32, device=H.device)
+        lse = torch.empty(0, dtype=torch.float32, device=H.device)
+        dH = torch.empty_like(H) if dH is None else dH
+        if dW is None:
+            dW = torch.empty(W.shape[0], W.shape[1], dtype=torch.float32, device=H.device)
+        dW.zero_()
+        allreduce_loss_and_dW(loss, dW, group)
+        return loss, lse, dH, dW
+    loss, lse, dH, dW = forward_backward(H, W, idx, logp, chunk, grad_scale=grad_scale, ws=ws, stream=stream,
+                                         weight=weight, dH=dH, dW=dW)
+    allreduce_loss_and_dW(loss, dW, group)
+    return loss, lse, dH, dW
 
 
 def teacher_topk(Ht, Wt, K, chunk, ws=None, stream=None, keep_logits=True):
