@@ -336,7 +336,29 @@ def cublas_context(w, dev, H, W_dev, idx, logp, reps=5):
     return out
 
 
-def path_summary(w, api, t_ms, steps, world, prof, peak_sus, peak_src):
+def kernel_work(w, kname):
+    """Algorithmic work of one step's launches of a product kernel: (FLOPs, DRAM bytes) per
+    step. Bytes count each operand once and each output once (dW's reduce-add launches read and
+    write dW: every chunk after the first); re-reads served by L2 are not algorithmic."""
+    n_chunks = -(-w.N // w.chunk)
+    rows = [min(w.chunk, w.N - c * w.chunk) for c in range(n_chunks)]
+    d, V = w.d, w.V
+    flops = sum(2.0 * r * d * V for r in rows)
+    Hc = sum(2.0 * r * d for r in rows)          # bf16 hidden states of each chunk
+    Wb = n_chunks * 2.0 * V * d                   # W read once per chunk
+    slab = sum(2.0 * r * V for r in rows)         # one pass over the bf16/fp16 slab
+    if kname == "bwd_dW_gemm":
+        byts = slab + Hc + 4.0 * V * d + (n_chunks - 1) * 8.0 * V * d
+    elif kname == "bwd_dH_gemm":
+        byts = slab + Wb + sum(4.0 * r * d for r in rows)
+    elif kname in ("fwd_logits_keep", "bwd_logit_grad"):
+        byts = Hc + Wb + slab
+    else:  # fwd_logits_lse: statistics only
+        byts = Hc + Wb + sum(12.0 * r * (-(-V // 256)) for r in rows)
+    return flops, byts
+
+
+def path_summary(w, api, t_ms, steps, world, prof, peak_sus, peak_src, hbm_peak=None):
     """Throughput of one timed path and the roofline of its dominant kernel.
 
     tflops_8NdV is the metric's count (8 N d V FLOPs per step: the four products of the
@@ -351,12 +373,25 @@ def path_summary(w, api, t_ms, steps, world, prof, peak_sus, peak_src):
     kname, (kms, kn) = max(prof.items(), key=lambda kv: kv[1][0])
     roof = None
     if kname in GEMM_KERNELS and kn > 0:
-        flops_per_launch = 2.0 * w.N * w.d * w.V * steps / kn
-        achieved = flops_per_launch / (kms / kn / 1e3) / 1e12
-        roof = {"kernel": kname, "bound": "tensor", "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
-                "frac": achieved / peak_sus, "traffic": profile_traffic(kname, w.name),
-                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step)",
-                "flops_per_launch": flops_per_launch, "avg_launch_ms": kms / kn}
+        # the kernel's own roofline: whichever of its FLOPs at the tensor peak and its
+        # algorithmic bytes at the HBM peak takes longer
+        f_step, b_step = kernel_work(w, kname)
+        per_step = kn / steps
+        flops_per_launch, bytes_per_launch = f_step / per_step, b_step / per_step
+        t_launch = kms / kn / 1e3
+        tfl = flops_per_launch / t_launch / 1e12
+        gbs = bytes_per_launch / t_launch / 1e9
+        hbm = hbm_peak or FALLBACK["hbm_gbs"]
+        tensor_bound = flops_per_launch / (peak_sus * 1e12) >= bytes_per_launch / (hbm * 1e9)
+        roof = {"kernel": kname, "bound": "tensor" if tensor_bound else "hbm",
+                "achieved": tfl if tensor_bound else gbs, "peak": peak_sus if tensor_bound else hbm,
+                "unit": "TFLOP/s" if tensor_bound else "GB/s",
+                "frac": tfl / peak_sus if tensor_bound else gbs / hbm,
+                "traffic": profile_traffic(kname, w.name),
+                "peak_source": (f"{peak_src} bf16 sustained (kernel timed inside a long step)" if tensor_bound
+                                else f"{peak_src} HBM copy bandwidth"),
+                "flops_per_launch": flops_per_launch, "algorithmic_bytes_per_launch": bytes_per_launch,
+                "tensor_frac": tfl / peak_sus, "hbm_frac": gbs / hbm, "avg_launch_ms": kms / kn}
     total = max(1e-9, sum(u[0] for u in prof.values()))
     return {"value": world * w.N * steps / (t_ms / 1e3), "ms_per_step": ms_step,
             "tflops_8NdV": tfl,
@@ -521,7 +556,8 @@ def run_ours(args):
 
     peaks, peak_src = measured_peaks()
     peak_sus = peak_value(peaks, "bf16_tflops_sustained")
-    head = path_summary(w, args.api, t_max, args.steps, world, prof, peak_sus, peak_src)
+    hbm_peak = peak_value(peaks, "hbm_gbs")
+    head = path_summary(w, args.api, t_max, args.steps, world, prof, peak_sus, peak_src, hbm_peak)
     line = {
         "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
@@ -541,7 +577,7 @@ def run_ours(args):
     }
     if other is not None:
         o_api, o_ms, o_launch, o_prof, o_clk = other
-        o = path_summary(w, o_api, o_ms, args.steps, world, o_prof, peak_sus, peak_src)
+        o = path_summary(w, o_api, o_ms, args.steps, world, o_prof, peak_sus, peak_src, hbm_peak)
         o.update({"api": o_api, "logits": config_of(w, o_api)["logits"], "gpu_launches": o_launch,
                   "clocks": o_clk, "steps": args.steps, "warmup": args.warmup})
         line[o_api] = o

@@ -252,13 +252,18 @@ __device__ __forceinline__ bool wait_phase_cluster(uint64_t* bar, uint32_t parit
   }
 }
 
-template <int CG, int BN, bool A_MN, bool B_MN, int EPI>
+// TF32: the operands are fp32 and the MMAs run as kind::tf32 (both operands K-major). A stage
+// then holds 32 fp32 values of K per row: the same 128 bytes, the same swizzled layout and the
+// same descriptors as 64 bf16 values, with four MMAs of K = 8 instead of K = 16.
+template <int CG, int BN, bool A_MN, bool B_MN, int EPI, bool TF32 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using L = TcSmem<CG, BN>;
   constexpr int NST = L::STAGES;
   constexpr int BN_CTA = L::BN_CTA;
+  constexpr int KE = TF32 ? BK / 2 : BK;  // K elements per stage (128 bytes of each row)
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per MMA");
   static_assert(!B_MN || BN_CTA % 64 == 0, "MN-major B is staged in 64-wide blocks");
+  static_assert(!TF32 || (!A_MN && !B_MN), "tf32 operands are staged K-major");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
@@ -344,13 +349,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
               tma_load_2d(dst, m, &full[s], x, y);
           };
           if (!A_MN) {
-            load(a, &p.tmA, kb * BK, arow);
+            load(a, &p.tmA, kb * KE, arow);
           } else {
 #pragma unroll
             for (int j = 0; j < BM / 64; ++j) load(a + j * 8192, &p.tmA, arow + 64 * j, kb * BK);
           }
           if (!B_MN) {
-            load(b, &p.tmB, kb * BK, bcol);
+            load(b, &p.tmB, kb * KE, bcol);
           } else {
 #pragma unroll
             for (int j = 0; j < BN_CTA / 64; ++j) load(b + j * 8192, &p.tmB, bcol + 64 * j, kb * BK);
@@ -372,7 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader CTA)
     if (lane == 0 && leader) {
-      constexpr uint32_t IDESC = make_idesc_bf16(BM * CG, BN, A_MN, B_MN);
+      constexpr uint32_t IDESC = TF32 ? make_idesc_tf32(BM * CG, BN) : make_idesc_bf16(BM * CG, BN, A_MN, B_MN);
       uint32_t cnt = 0, it = 0;
       bool ok = true;
       for (int u = cluster_id; ok && u < p.num_units; u += num_clusters, ++it) {
@@ -399,10 +404,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                                      : make_sdesc_sw128(a_addr + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? make_sdesc_sw128(b_addr + kk * 2048, 8192, 1024)
                                      : make_sdesc_sw128(b_addr + kk * 32, 16, 1024);
-            if constexpr (CG == 2)
-              umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+            const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
+            if constexpr (CG == 2 && TF32)
+              umma_tf32_pair(d_tmem, ad, bd, IDESC, accum);
+            else if constexpr (CG == 2)
+              umma_bf16_pair(d_tmem, ad, bd, IDESC, accum);
+            else if constexpr (TF32)
+              umma_tf32(d_tmem, ad, bd, IDESC, accum);
             else
-              umma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+              umma_bf16(d_tmem, ad, bd, IDESC, accum);
           }
           if constexpr (CG == 2)
             umma_commit_pair(&empty[s], 0x3);
@@ -648,15 +658,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           }
         }
       } else {
-        // EPI_STORE_F32
+        // EPI_STORE_F32. Two staging buffers per warp, at most one store reading shared memory
+        // at a time: box j is staged while store j-1 drains, and store j is issued once store
+        // j-1 has read its buffer (which also frees the buffer box j+1 reuses). Stores issued in
+        // bursts delay the next unit's operand loads, which share the SM's path to L2; paced,
+        // the fp32 output stream of dW costs the main loop less.
         if (!warp_wait_phase(&tfull[acc], use & 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const int y = sp * p.c_split_rows + row0;
 #pragma unroll 1
         for (int j = 0; j < BN / 32; ++j, ++ecnt) {
           uint8_t* buf = ebuf0 + (ecnt & 1u) * EPI_BUF_BYTES;
-          if (ecnt >= 2 && lane == 0) bulk_wait_read<1>();
-          __syncwarp();
+          __syncwarp();  // lane 0 has seen store ecnt-2 read this buffer (before issuing ecnt-1)
           float x[32];
           tmem_ld32(taddr + 32 * j, x);
           if (j == BN / 32 - 1) release_acc(acc);
@@ -669,6 +682,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
+            bulk_wait_read<0>();  // store ecnt-1 has read its buffer
             const int sx = nb * BN + 32 * j;
             if (sx < p.c_xlim && y < p.c_ylim) {
               if (p.c_reduce)
