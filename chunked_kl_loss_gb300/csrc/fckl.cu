@@ -52,7 +52,7 @@ enum Kind {
 };
 const char* const kKindNames[KIND_COUNT] = {"preprocess",     "fwd_logits_lse", "fwd_combine",
                                             "loss_reduce",    "bwd_logit_grad", "bwd_dH_gemm",
-                                            "bwd_dH_reduce",  "bwd_dW_gemm",    "cvt_bf16",
+                                            "bwd_dH_reduce",  "bwd_dW_gemm",    "cvt_inputs",
                                             "wait_timeout_selftest", "topk_logits_stats", "topk_threshold",
                                             "topk_collect",           "topk_select",
                                             "fwd_logits_keep",        "bwd_grad_from_logits",
@@ -214,7 +214,7 @@ struct Plan {
   int ldG;         // row pitch (elements) of the bf16 gradient slab
   int bn_d;        // N-tile of the dH / dW products
   size_t off_status, off_sidx, off_sp, off_S, off_T, off_pm, off_pl, off_pc, off_rowloss, off_G, off_dhp,
-      off_Hb, off_Wb, total;
+      off_Hb, off_Wb, off_Ht, off_Wt, total;
 };
 
 // N-tile of the dH and dW products (over d). 256 columns: an SM pair stages 128 each, two
@@ -266,6 +266,8 @@ Plan make_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
   p.off_dhp = take(static_cast<size_t>(MAX_SPLITS) * R * d * 4);
   p.off_Hb = dt == FCKL_F32 ? take(R * d * 2) : o;
   p.off_Wb = dt == FCKL_F32 ? take(static_cast<size_t>(V) * d * 2) : o;
+  p.off_Ht = dt == FCKL_F32 ? take(R * d * 4) : o;
+  p.off_Wt = dt == FCKL_F32 ? take(static_cast<size_t>(V) * d * 4) : o;
   p.total = o;
   return p;
 }
@@ -281,9 +283,9 @@ constexpr int TILE_M = BM * CG;  // rows of one MMA tile
 
 // Persistent launch: one CTA (pair) per SM (pair), as many as can be resident, capped by the
 // number of work units.
-template <int BN, bool AMN, bool BMN, int EPI>
+template <int BN, bool AMN, bool BMN, int EPI, bool TF32 = false>
 int launch_tc(int kind, DevInfo* di, const TcParams& p, cudaStream_t s, const char* what) {
-  auto k = tc_gemm_kernel<CG, BN, AMN, BMN, EPI>;
+  auto k = tc_gemm_kernel<CG, BN, AMN, BMN, EPI, TF32>;
   constexpr uint32_t smem = TcSmem<CG, BN>::DYN_BYTES;
   static_assert(smem <= 232448, "shared memory budget");
   static bool attr_done[64] = {};  // one flag per device for this instantiation
@@ -324,10 +326,13 @@ int launch_tc(int kind, DevInfo* di, const TcParams& p, cudaStream_t s, const ch
   return launch(kind, s, what, [&] { cudaLaunchKernelEx(&cfg, k, p); });
 }
 
-int launch_cvt(const float* src, void* dst, int64_t n, DevInfo* di, cudaStream_t s) {
+// Copies of fp32 inputs: tf32-rounded into t32 (for the logits products) and/or bf16 into b16
+// (for the dH and dW products); either may be null.
+int launch_cvt(const float* src, void* t32, void* b16, int64_t n, DevInfo* di, cudaStream_t s) {
   const int grid = static_cast<int>(std::min<int64_t>(cdiv(n / 4, 256), int64_t(di->sms) * 8));
-  return launch(KIND_CVT, s, "cvt_bf16", [&] {
-    cvt_bf16_kernel<<<std::max(grid, 1), 256, 0, s>>>(src, static_cast<__nv_bfloat16*>(dst), n);
+  return launch(KIND_CVT, s, "cvt_inputs", [&] {
+    cvt_inputs_kernel<<<std::max(grid, 1), 256, 0, s>>>(src, static_cast<float*>(t32),
+                                                        static_cast<__nv_bfloat16*>(b16), n);
   });
 }
 
@@ -374,7 +379,8 @@ struct Run {
   uint8_t* w = nullptr;  // workspace
   unsigned* status = nullptr;
   const void* H = nullptr;
-  const void* Wb = nullptr;  // W as bf16 (the caller's W, or its bf16 copy)
+  const void* Wraw = nullptr;  // the caller's W (bf16, or fp32 read as tf32 by the logits products)
+  const void* Wb = nullptr;  // W as bf16 (the caller's W, or its bf16 copy for the dH product)
   int dtype = FCKL_BF16;
   const int32_t* idx = nullptr;
   const float* logp = nullptr;
@@ -398,14 +404,24 @@ int run_begin(Run& r, bool backward) {
     return FCKL_ERR_CUDA;
   }
   int st;
-  if (r.dtype == FCKL_F32) {
-    if ((st = launch_cvt(static_cast<const float*>(r.Wb), r.w + pl.off_Wb, int64_t(pl.V) * pl.d, r.di, r.s)))
+  if (r.dtype == FCKL_F32) {  // tf32 copy for the logits products, bf16 copy for the dH product
+    if ((st = launch_cvt(static_cast<const float*>(r.Wraw), r.w + pl.off_Wt, backward ? r.w + pl.off_Wb : nullptr,
+                         int64_t(pl.V) * pl.d, r.di, r.s)))
       return st;
-    r.Wb = r.w + pl.off_Wb;
+    r.Wraw = r.w + pl.off_Wt;
+    if (backward) r.Wb = r.w + pl.off_Wb;
   }
   const int d = pl.d, V = pl.V;
-  if ((st = make_map(&r.tmW_k, r.Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK, VOCAB_TILE / CG)))
+  // The logits products read W K-major: bf16, or the tf32-rounded copy of an fp32 W (32
+  // values per 128-byte stage row).
+  if (r.dtype == FCKL_F32) {
+    if ((st = make_map(&r.tmW_k, r.Wraw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, V, uint64_t(d) * 4, BK / 2,
+                       VOCAB_TILE / CG)))
+      return st;
+  } else if ((st = make_map(&r.tmW_k, r.Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK,
+                            VOCAB_TILE / CG))) {
     return st;
+  }
   if (!backward) return FCKL_OK;
   if ((st = make_map(&r.tmW_mn, r.Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, 64, BK))) return st;
   if ((st = make_map(&r.tmDW, r.dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, V, uint64_t(d) * 4, 32, 32))) return st;
@@ -430,35 +446,49 @@ int run_begin(Run& r, bool backward) {
   return FCKL_OK;
 }
 
-// Orders the chunk's cache slots (and rounds an fp32 chunk of H); returns the chunk's H rows.
-int chunk_prepare(Run& r, int64_t r0, int rows, const void** Hc) {
+// Orders the chunk's cache slots; returns the chunk's H rows as the logits products read them
+// (*Hl: bf16, or for fp32 inputs a tf32-rounded copy) and as the dW product reads them (*Hc:
+// bf16; for fp32 inputs a bf16 copy, made only when `backward`).
+int chunk_prepare(Run& r, int64_t r0, int rows, const void** Hl, const void** Hc, bool backward) {
   const Plan& pl = r.pl;
   int st = launch_preprocess(pl, r.idx + r0 * pl.K, r.logp + r0 * pl.K, rows, r.w, r.status, r.di, r.s);
   if (st) return st;
   const size_t esz = r.dtype == FCKL_F32 ? 4 : 2;
-  *Hc = static_cast<const uint8_t*>(r.H) + static_cast<size_t>(r0) * pl.d * esz;
+  *Hl = static_cast<const uint8_t*>(r.H) + static_cast<size_t>(r0) * pl.d * esz;
+  *Hc = *Hl;
   if (r.dtype == FCKL_F32) {
-    if ((st = launch_cvt(static_cast<const float*>(*Hc), r.w + pl.off_Hb, int64_t(rows) * pl.d, r.di, r.s)))
+    if ((st = launch_cvt(static_cast<const float*>(*Hl), r.w + pl.off_Ht, backward ? r.w + pl.off_Hb : nullptr,
+                         int64_t(rows) * pl.d, r.di, r.s)))
       return st;
+    *Hl = r.w + pl.off_Ht;
     *Hc = r.w + pl.off_Hb;
   }
   return FCKL_OK;
 }
 
+// Map of a chunk's hidden states as the logits products read them (K-major, 128 rows a box).
+int map_logits_A(const Run& r, CUtensorMap* m, const void* Hl, int rows) {
+  const int d = r.pl.d;
+  if (r.dtype == FCKL_F32)
+    return make_map(m, Hl, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, rows, uint64_t(d) * 4, BK / 2, BM);
+  return make_map(m, Hl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM);
+}
+// K-blocks of the logits products: 64 bf16 or 32 fp32 values of d per stage.
+int logits_kblocks(const Run& r) { return static_cast<int>(cdiv(r.pl.d, r.dtype == FCKL_F32 ? BK / 2 : BK)); }
+
 // Forward of one chunk: logits tiles -> per-tile (max, sum-exp, gathered sum) -> lse and loss.
 // With keep, exp(z - tile max) is also stored (fp16) into the gradient slab for the chunk's
 // backward.
-int chunk_forward(Run& r, int64_t r0, int rows, const void* Hc, bool keep = false) {
+int chunk_forward(Run& r, int64_t r0, int rows, const void* Hl, bool keep = false) {
   const Plan& pl = r.pl;
-  const int d = pl.d;
   uint8_t* w = r.w;
   int st;
   TcParams p;
   memset(&p, 0, sizeof(p));
-  if ((st = make_map(&p.tmA, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM))) return st;
+  if ((st = map_logits_A(r, &p.tmA, Hl, rows))) return st;
   p.tmB = r.tmW_k;
-  p.sch = {static_cast<int>(cdiv(rows, TILE_M)), pl.tiles_v, static_cast<int>(cdiv(d, BK)), 1,
-           static_cast<int>(cdiv(d, BK)), 1};
+  const int kbl = logits_kblocks(r);
+  p.sch = {static_cast<int>(cdiv(rows, TILE_M)), pl.tiles_v, kbl, 1, kbl, 1};
   p.num_units = p.sch.m_blocks * p.sch.n_blocks;
   p.status = r.status;
   p.rows_valid = rows;
@@ -477,9 +507,15 @@ int chunk_forward(Run& r, int64_t r0, int rows, const void* Hc, bool keep = fals
       return st;
     p.c_xlim = pl.V;
     p.c_ylim = rows;
-    st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_KEEP>(KIND_FWD_LOGITS_KEEP, r.di, p, r.s, "fwd_logits_keep");
+    st = r.dtype == FCKL_F32
+             ? launch_tc<VOCAB_TILE, false, false, EPI_FWD_KEEP, true>(KIND_FWD_LOGITS_KEEP, r.di, p, r.s,
+                                                                       "fwd_logits_keep")
+             : launch_tc<VOCAB_TILE, false, false, EPI_FWD_KEEP>(KIND_FWD_LOGITS_KEEP, r.di, p, r.s, "fwd_logits_keep");
   } else {
-    st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_STATS>(KIND_FWD_LOGITS, r.di, p, r.s, "fwd_logits_lse");
+    st = r.dtype == FCKL_F32
+             ? launch_tc<VOCAB_TILE, false, false, EPI_FWD_STATS, true>(KIND_FWD_LOGITS, r.di, p, r.s,
+                                                                        "fwd_logits_lse")
+             : launch_tc<VOCAB_TILE, false, false, EPI_FWD_STATS>(KIND_FWD_LOGITS, r.di, p, r.s, "fwd_logits_lse");
   }
   if (st) return st;
   const int cblocks = static_cast<int>(cdiv(rows, 32));
@@ -494,9 +530,9 @@ int chunk_forward(Run& r, int64_t r0, int rows, const void* Hc, bool keep = fals
 }
 
 // G = scale * w_n * (S softmax(z) - p_sparse) of one chunk, from its recomputed logits.
-int grad_recompute(Run& r, int64_t r0, int rows, const void* Hc) {
+int grad_recompute(Run& r, int64_t r0, int rows, const void* Hl) {
   const Plan& pl = r.pl;
-  const int d = pl.d, V = pl.V;
+  const int V = pl.V;
   uint8_t* w = r.w;
   cudaStream_t s = r.s;
   void* G = w + pl.off_G;
@@ -504,11 +540,12 @@ int grad_recompute(Run& r, int64_t r0, int rows, const void* Hc) {
   int st;
   TcParams pg;
   memset(&pg, 0, sizeof(pg));
-  if ((st = make_map(&pg.tmA, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM))) return st;
+  if ((st = map_logits_A(r, &pg.tmA, Hl, rows))) return st;
   pg.tmB = r.tmW_k;
   if ((st = make_map(&pg.tmC, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, uint64_t(pl.ldG) * 2, 64, 32)))
     return st;
-  pg.sch = {mbr, pl.tiles_v, static_cast<int>(cdiv(d, BK)), 1, static_cast<int>(cdiv(d, BK)), 1};
+  const int kbl = logits_kblocks(r);
+  pg.sch = {mbr, pl.tiles_v, kbl, 1, kbl, 1};
   pg.num_units = mbr * pl.tiles_v;
   pg.status = r.status;
   pg.rows_valid = rows;
@@ -522,6 +559,8 @@ int grad_recompute(Run& r, int64_t r0, int rows, const void* Hc) {
   pg.gscale = r.grad_scale;
   pg.c_xlim = V;
   pg.c_ylim = rows;
+  if (r.dtype == FCKL_F32)
+    return launch_tc<VOCAB_TILE, false, false, EPI_LOGIT_GRAD, true>(KIND_BWD_GRAD, r.di, pg, s, "bwd_logit_grad");
   return launch_tc<VOCAB_TILE, false, false, EPI_LOGIT_GRAD>(KIND_BWD_GRAD, r.di, pg, s, "bwd_logit_grad");
 }
 
@@ -551,7 +590,7 @@ int grad_from_kept(Run& r, int64_t r0, int rows) {
 
 // Backward of one chunk: G from recomputed logits (or, with keep, from what the chunk's forward
 // kept in the slab), then dH_chunk = G W and dW (+)= G^T H_chunk.
-int chunk_backward(Run& r, int64_t r0, int rows, const void* Hc, bool keep = false) {
+int chunk_backward(Run& r, int64_t r0, int rows, const void* Hl, const void* Hc, bool keep = false) {
   const Plan& pl = r.pl;
   const int d = pl.d, V = pl.V;
   uint8_t* w = r.w;
@@ -563,7 +602,7 @@ int chunk_backward(Run& r, int64_t r0, int rows, const void* Hc, bool keep = fal
   int st;
 
   // --- G = scale * w_n * (S softmax(z) - p_sparse), z kept or recomputed
-  if ((st = keep ? grad_from_kept(r, r0, rows) : grad_recompute(r, r0, rows, Hc))) return st;
+  if ((st = keep ? grad_from_kept(r, r0, rows) : grad_recompute(r, r0, rows, Hl))) return st;
 
   // --- dH_chunk = G W, split over the vocabulary into fp32 partials, then summed
   const int nbd = static_cast<int>(cdiv(d, pl.bn_d));
@@ -637,6 +676,7 @@ int run_setup(Run& r, const void* H, const void* W, int dtype, const int32_t* id
   r.w = static_cast<uint8_t*>(ws);
   r.status = reinterpret_cast<unsigned*>(r.w + r.pl.off_status);
   r.H = H;
+  r.Wraw = W;
   r.Wb = W;
   r.dtype = dtype;
   r.idx = idx;
@@ -653,7 +693,7 @@ struct TopkPlan {
   int chunk, rows_alloc, tiles_v, cmax;
   int thr_rows, thr_stride;  // threshold kernel: positions per block, shared-memory row pitch
   int ldz;  // row pitch (elements) of the kept logits
-  size_t off_status, off_pm, off_pl, off_pc, off_lse, off_thr, off_cnt, off_cv, off_cz, off_Hb, off_Wb, total;
+  size_t off_status, off_pm, off_pl, off_pc, off_lse, off_thr, off_cnt, off_cv, off_cz, off_Ht, off_Wt, total;
   // the chunk's fp32 logits from pass 1, read by the collect step, and per position the list
   // of tiles whose maximum reaches the threshold
   size_t off_Z, off_live, off_live_cnt, total_keep;
@@ -684,8 +724,8 @@ TopkPlan make_topk_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
   p.off_cnt = take(R * 4);
   p.off_cv = take(R * p.cmax * 4);
   p.off_cz = take(R * p.cmax * 4);
-  p.off_Hb = dt == FCKL_F32 ? take(R * d * 2) : o;
-  p.off_Wb = dt == FCKL_F32 ? take(static_cast<size_t>(V) * d * 2) : o;
+  p.off_Ht = dt == FCKL_F32 ? take(R * d * 4) : o;
+  p.off_Wt = dt == FCKL_F32 ? take(static_cast<size_t>(V) * d * 4) : o;
   p.total = o;
   p.ldz = static_cast<int>(rup(V, 8));
   p.off_Z = take(R * p.ldz * 4);
@@ -720,9 +760,9 @@ int fckl_forward(const void* H, const void* W, int dtype, const int32_t* idx, co
   if ((st = run_begin(r, false))) return st;
   for (int64_t r0 = 0; r0 < N; r0 += r.pl.chunk) {
     const int rows = static_cast<int>(std::min<int64_t>(r.pl.chunk, N - r0));
-    const void* Hc = nullptr;
-    if ((st = chunk_prepare(r, r0, rows, &Hc))) return st;
-    if ((st = chunk_forward(r, r0, rows, Hc))) return st;
+    const void *Hl = nullptr, *Hc = nullptr;
+    if ((st = chunk_prepare(r, r0, rows, &Hl, &Hc, false))) return st;
+    if ((st = chunk_forward(r, r0, rows, Hl))) return st;
   }
   return run_loss(r, loss);
 }
@@ -741,9 +781,9 @@ int fckl_backward(const void* H, const void* W, int dtype, const int32_t* idx, c
   if ((st = run_begin(r, true))) return st;
   for (int64_t r0 = 0; r0 < N; r0 += r.pl.chunk) {
     const int rows = static_cast<int>(std::min<int64_t>(r.pl.chunk, N - r0));
-    const void* Hc = nullptr;
-    if ((st = chunk_prepare(r, r0, rows, &Hc))) return st;
-    if ((st = chunk_backward(r, r0, rows, Hc))) return st;
+    const void *Hl = nullptr, *Hc = nullptr;
+    if ((st = chunk_prepare(r, r0, rows, &Hl, &Hc, true))) return st;
+    if ((st = chunk_backward(r, r0, rows, Hl, Hc))) return st;
   }
   return FCKL_OK;
 }
@@ -766,10 +806,10 @@ int fckl_forward_backward(const void* H, const void* W, int dtype, const int32_t
   if ((st = run_begin(r, true))) return st;
   for (int64_t r0 = 0; r0 < N; r0 += r.pl.chunk) {
     const int rows = static_cast<int>(std::min<int64_t>(r.pl.chunk, N - r0));
-    const void* Hc = nullptr;
-    if ((st = chunk_prepare(r, r0, rows, &Hc))) return st;
-    if ((st = chunk_forward(r, r0, rows, Hc, true))) return st;
-    if ((st = chunk_backward(r, r0, rows, Hc, true))) return st;
+    const void *Hl = nullptr, *Hc = nullptr;
+    if ((st = chunk_prepare(r, r0, rows, &Hl, &Hc, true))) return st;
+    if ((st = chunk_forward(r, r0, rows, Hl, true))) return st;
+    if ((st = chunk_backward(r, r0, rows, Hl, Hc, true))) return st;
   }
   return run_loss(r, loss);
 }
@@ -834,14 +874,18 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
     set_error("cudaMemsetAsync", e);
     return FCKL_ERR_CUDA;
   }
-  const void* Wb = Wt;
-  if (dtype == FCKL_F32) {
-    if ((st = launch_cvt(static_cast<const float*>(Wt), w + tp.off_Wb, int64_t(V) * d, di, s))) return st;
-    Wb = w + tp.off_Wb;
+  // Both passes are logits products: bf16 operands, or tf32-rounded copies of fp32 ones.
+  const bool f32 = dtype == FCKL_F32;
+  const CUtensorMapDataType mdt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint32_t ke = f32 ? BK / 2 : BK;  // K values per 128-byte stage row
+  const size_t esz = f32 ? 4 : 2;
+  const void* Wl = Wt;
+  if (f32) {
+    if ((st = launch_cvt(static_cast<const float*>(Wt), w + tp.off_Wt, nullptr, int64_t(V) * d, di, s))) return st;
+    Wl = w + tp.off_Wt;
   }
   CUtensorMap tmW;
-  if ((st = make_map(&tmW, Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK, VOCAB_TILE / CG)))
-    return st;
+  if ((st = make_map(&tmW, Wl, mdt, d, V, uint64_t(d) * esz, ke, VOCAB_TILE / CG))) return st;
   float* pm = reinterpret_cast<float*>(w + tp.off_pm);
   float* pl = reinterpret_cast<float*>(w + tp.off_pl);
   float* lse = reinterpret_cast<float*>(w + tp.off_lse);
@@ -849,21 +893,21 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
   int* cnt = reinterpret_cast<int*>(w + tp.off_cnt);
   int* cv = reinterpret_cast<int*>(w + tp.off_cv);
   float* cz = reinterpret_cast<float*>(w + tp.off_cz);
-  const size_t esz = dtype == FCKL_F32 ? 4 : 2;
+  const int kbl = static_cast<int>(cdiv(d, ke));
   for (int64_t r0 = 0; r0 < N; r0 += tp.chunk) {
     const int rows = static_cast<int>(std::min<int64_t>(tp.chunk, N - r0));
     const void* Hc = static_cast<const uint8_t*>(Ht) + static_cast<size_t>(r0) * d * esz;
-    if (dtype == FCKL_F32) {
-      if ((st = launch_cvt(static_cast<const float*>(Hc), w + tp.off_Hb, int64_t(rows) * d, di, s))) return st;
-      Hc = w + tp.off_Hb;
+    if (f32) {
+      if ((st = launch_cvt(static_cast<const float*>(Hc), w + tp.off_Ht, nullptr, int64_t(rows) * d, di, s)))
+        return st;
+      Hc = w + tp.off_Ht;
     }
     // pass 1: per (row, vocabulary tile) max and sum-exp
     TcParams p;
     memset(&p, 0, sizeof(p));
-    if ((st = make_map(&p.tmA, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM))) return st;
+    if ((st = make_map(&p.tmA, Hc, mdt, d, rows, uint64_t(d) * esz, ke, BM))) return st;
     p.tmB = tmW;
-    p.sch = {static_cast<int>(cdiv(rows, TILE_M)), tp.tiles_v, static_cast<int>(cdiv(d, BK)), 1,
-             static_cast<int>(cdiv(d, BK)), 1};
+    p.sch = {static_cast<int>(cdiv(rows, TILE_M)), tp.tiles_v, kbl, 1, kbl, 1};
     p.num_units = p.sch.m_blocks * p.sch.n_blocks;
     p.status = status;
     p.rows_valid = rows;
@@ -879,9 +923,13 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
         return st;
       p.c_xlim = V;
       p.c_ylim = rows;
-      st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_Z>(KIND_TOPK_LOGITS_KEEP, di, p, s, "topk_logits_keep");
+      st = f32 ? launch_tc<VOCAB_TILE, false, false, EPI_FWD_Z, true>(KIND_TOPK_LOGITS_KEEP, di, p, s,
+                                                                      "topk_logits_keep")
+               : launch_tc<VOCAB_TILE, false, false, EPI_FWD_Z>(KIND_TOPK_LOGITS_KEEP, di, p, s, "topk_logits_keep");
     } else {
-      st = launch_tc<VOCAB_TILE, false, false, EPI_FWD_STATS>(KIND_TOPK_LOGITS, di, p, s, "topk_logits_stats");
+      st = f32 ? launch_tc<VOCAB_TILE, false, false, EPI_FWD_STATS, true>(KIND_TOPK_LOGITS, di, p, s,
+                                                                          "topk_logits_stats")
+               : launch_tc<VOCAB_TILE, false, false, EPI_FWD_STATS>(KIND_TOPK_LOGITS, di, p, s, "topk_logits_stats");
     }
     if (st) return st;
     const int wblocks = static_cast<int>(cdiv(rows, 4));
@@ -911,7 +959,9 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
       p.cand_v = cv;
       p.cand_z = cz;
       p.cmax = cmax;
-      st = launch_tc<VOCAB_TILE, false, false, EPI_TOPK_COLLECT>(KIND_TOPK_COLLECT, di, p, s, "topk_collect");
+      st = f32 ? launch_tc<VOCAB_TILE, false, false, EPI_TOPK_COLLECT, true>(KIND_TOPK_COLLECT, di, p, s,
+                                                                             "topk_collect")
+               : launch_tc<VOCAB_TILE, false, false, EPI_TOPK_COLLECT>(KIND_TOPK_COLLECT, di, p, s, "topk_collect");
     }
     if (st) return st;
     int32_t* io = idx + r0 * K;

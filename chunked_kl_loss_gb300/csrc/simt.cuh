@@ -1,6 +1,6 @@
 // SIMT kernels around the tensor-core steps: teacher-cache preparation, the merge of the
 // per-vocabulary-tile statistics into lse and the per-position loss, the fixed-order loss
-// sum, the split-K sum of dH, and fp32 -> bf16 rounding of fp32 inputs.
+// sum, the split-K sum of dH, and the tf32 / bf16 copies of fp32 inputs.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -474,13 +474,27 @@ __global__ void __launch_bounds__(GRAD_THREADS) logit_grad_kernel(
   }
 }
 
-// fp32 -> bf16, round to nearest even; n % 4 == 0.
-__global__ void __launch_bounds__(256) cvt_bf16_kernel(const float* __restrict__ src,
-                                                       __nv_bfloat16* __restrict__ dst, int64_t n) {
+// fp32 -> tf32 (10 explicit mantissa bits, round to nearest with ties away from zero), kept
+// in an fp32 container with the low 13 bits zero: the value the tf32 tensor-core products
+// then read exactly (they would otherwise drop the low bits, a bias toward zero).
+__device__ __forceinline__ float round_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+// fp32 inputs, one read: tf32-rounded copy into t32 and/or bf16 copy (round to nearest even)
+// into b16 (either may be null); n % 4 == 0.
+__global__ void __launch_bounds__(256) cvt_inputs_kernel(const float* __restrict__ src, float* __restrict__ t32,
+                                                         __nv_bfloat16* __restrict__ b16, int64_t n) {
   const int64_t n4 = n / 4;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    store4(dst + 4 * i, *reinterpret_cast<const float4*>(src + 4 * i));
+    const float4 v = *reinterpret_cast<const float4*>(src + 4 * i);
+    if (t32)
+      *reinterpret_cast<float4*>(t32 + 4 * i) =
+          make_float4(round_tf32(v.x), round_tf32(v.y), round_tf32(v.z), round_tf32(v.w));
+    if (b16) store4(b16 + 4 * i, v);
   }
 }
 

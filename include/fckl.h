@@ -24,9 +24,13 @@
  *    allocates no device memory at run time (the one exception is the fixed scratch array
  *    of fckl_forward_static, reserved when the library is loaded) and keeps only host-side
  *    caches (device properties, one-time kernel set-up).
- *  - H is [N, d] and W is [V, d], both of type `dtype` (FCKL_BF16 or FCKL_F32). FCKL_F32
- *    inputs are rounded to bf16 on the device and the tensor-core products run in bf16
- *    with fp32 accumulation, exactly as for FCKL_BF16 inputs.
+ *  - H is [N, d] and W is [V, d], both of type `dtype` (FCKL_BF16 or FCKL_F32). With FCKL_F32
+ *    the logits products (the forward projection, the backward's recompute, both passes of
+ *    the top-K builder) run on the tensor cores as tf32 with fp32 accumulation, on copies of
+ *    W and of each chunk of H rounded to tf32 (10 explicit mantissa bits, to nearest, ties
+ *    away from zero) in the workspace. G is rounded to bf16 as for bf16 inputs, and the dH
+ *    and dW products read bf16 copies of W and of each chunk of H (round to nearest even).
+ *    FCKL_BF16 inputs run every product in bf16 with fp32 accumulation.
  *  - idx is int32 [N, K]: teacher token ids, any order, each in [0, V). logp is fp32 [N, K]:
  *    the teacher's log-probabilities for those ids; -inf marks an empty slot. A repeated
  *    id within a row contributes once per slot.

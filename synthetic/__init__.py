@@ -40,7 +40,7 @@ import dataclasses
 import numpy as np
 
 __all__ = ["Workload", "WORKLOADS", "hidden_states", "output_projection",
-           "teacher_cache", "make_inputs"]
+           "teacher_cache", "make_inputs", "round_bf16", "round_tf32"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -125,6 +125,15 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
     """Round fp32 values to bf16 (nearest even) and return them as fp32."""
     import torch
     return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).to(torch.float32).numpy()
+
+
+def round_tf32(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to tf32 (10 explicit mantissa bits) to nearest, ties away from zero,
+    and return them as fp32 with the low 13 bits zero: the values a tf32 product reads. Adding
+    half a tf32 unit (bit 12) to the magnitude bits and clearing the 13 low bits rounds the
+    magnitude; a carry into the exponent is the correct rounding up. Finite inputs."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + 0x1000) & 0xFFFFE000).astype(np.uint32).view(np.float32)
 
 
 def make_inputs(N: int, d: int, V: int, K: int, dtype: str = "bf16", seed: int = 0):

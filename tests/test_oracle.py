@@ -386,3 +386,20 @@ def test_empty_row_and_one_hot_row_closed_forms():
         G_all[n] = np.exp(lq[n])
         G_all[n, idx[n, k]] -= 1.0
     np.testing.assert_allclose(dW, G_all.T @ H, rtol=1e-10, atol=1e-12)
+
+
+def test_tf32_rounding_of_inputs():
+    """synthetic.round_tf32 against a frexp restatement: nearest value with 11 significant bits,
+    ties away from zero."""
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.standard_normal(10000).astype(np.float32) * 10 ** rng.uniform(-6, 6, 10000),
+                        np.float32([0.0, -0.0, 1.0, -1.0, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11,
+                                    -(1.0 + 2.0 ** -11), 2.0 - 2.0 ** -12])]).astype(np.float32)
+    m, e = np.frexp(x.astype(np.float64))            # |m| in [0.5, 1): 11 bits are m * 2^11
+    q = np.floor(np.abs(m) * 2.0 ** 11 + 0.5) * np.sign(m)
+    ref = np.ldexp(q / 2.0 ** 11, e)
+    got = synthetic.round_tf32(x).astype(np.float64)
+    assert np.array_equal(got, ref)
+    # exact ties round away from zero; the largest value below 2 rounds up to 2
+    assert synthetic.round_tf32(np.float32([1.0 + 2.0 ** -11]))[0] == np.float32(1.0 + 2.0 ** -10)
+    assert synthetic.round_tf32(np.float32([2.0 - 2.0 ** -12]))[0] == np.float32(2.0)

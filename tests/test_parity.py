@@ -65,6 +65,28 @@ def test_tiny_workload_fp32(fckl):
     assert_parity(got, x, w.chunk)
 
 
+def test_fp32_inputs_run_tf32_logits(fckl):
+    """fp32 inputs: the logits products run as tf32 on rounded copies. Against the oracle on the
+    tf32-rounded inputs (what the products compute) lse and the per-position loss agree to
+    fp32 accumulation error; against the exact fp32 inputs lse is several times closer than
+    the bf16 path gets on the same inputs, and the gradients meet the method's tolerance."""
+    w = synthetic.WORKLOADS["tiny_n64_d256_v4096"]
+    x = synthetic.make_inputs(w.N, w.d, w.V, w.K, dtype="f32", seed=0)
+    loss, lse, rl, dH, dW = run_gpu(fckl, x, w.chunk, "f32")
+    xt = dict(x, H=synthetic.round_tf32(x["H"]), W=synthetic.round_tf32(x["W"]))
+    t_loss, t_lse, t_rl = orc.forward(xt["H"], xt["W"], xt["idx"], xt["logp"], w.chunk)
+    assert abs(loss - t_loss) <= 1e-5 * abs(t_loss)
+    assert np.abs(lse - t_lse).max() <= 1e-4
+    assert np.abs(rl - t_rl).max() <= 1e-4 * (1 + np.abs(t_rl).max())
+    r_loss, r_lse, _ = orc.forward(x["H"], x["W"], x["idx"], x["logp"], w.chunk)
+    e_tf32 = np.abs(lse - r_lse).max()
+    b_loss, b_lse, _, _, _ = run_gpu(fckl, dict(x, H=synthetic.round_bf16(x["H"]), W=synthetic.round_bf16(x["W"])),
+                                     w.chunk, "bf16")
+    e_bf16 = np.abs(b_lse - r_lse).max()
+    assert e_tf32 <= 0.5 * e_bf16, (e_tf32, e_bf16)
+    assert_parity((loss, lse, rl, dH, dW), x, w.chunk)
+
+
 @pytest.mark.parametrize("N,d,V,K,chunk", [
     (300, 320, 5000, 40, 128),    # ragged N, chunk tail of 44 rows, V tail, d tail vs a 256 tile
     (256, 512, 4096, 16, 256),    # exact tiles
