@@ -283,46 +283,61 @@ constexpr int TILE_M = BM * CG;  // rows of one MMA tile
 
 // Persistent launch: one CTA (pair) per SM (pair), as many as can be resident, capped by the
 // number of work units.
+// Launch configuration of one engine instantiation: one CTA (pair) per SM (pair), as many
+// clusters as can be resident at once. The first call on a device sets the shared-memory limit
+// and asks the occupancy calculator; *clusters receives the resident cluster count.
 template <int BN, bool AMN, bool BMN, int EPI, bool TF32 = false>
-int launch_tc(int kind, DevInfo* di, const TcParams& p, cudaStream_t s, const char* what) {
+int tc_setup(DevInfo* di, cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int* clusters) {
   auto k = tc_gemm_kernel<CG, BN, AMN, BMN, EPI, TF32>;
   constexpr uint32_t smem = TcSmem<CG, BN>::DYN_BYTES;
   static_assert(smem <= 232448, "shared memory budget");
   static bool attr_done[64] = {};  // one flag per device for this instantiation
   static int max_clusters[64] = {};
   const int dev = di->id;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  *cfg = cudaLaunchConfig_t{};
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CG;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = CG > 1 ? 1 : 0;
+  cfg->blockDim = dim3(NUM_THREADS);
+  cfg->dynamicSmemBytes = smem;
+  cfg->attrs = attr;
+  cfg->numAttrs = CG > 1 ? 1 : 0;
   {
     std::lock_guard<std::mutex> lk(g_setup_mu);  // one-time per-device set-up, any host thread
     if (!attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) {
-      set_error("cudaFuncSetAttribute", e);
-      return FCKL_ERR_CUDA;
-    }
-    int n = di->sms / CG;
-    if (CG > 1) {
-      cfg.gridDim = dim3(static_cast<unsigned>(CG * n));
-      int m = 0;
-      if (cudaOccupancyMaxActiveClusters(&m, k, &cfg) == cudaSuccess && m > 0) n = std::min(n, m);
-      cudaGetLastError();
-    }
-    max_clusters[dev] = n;
-    attr_done[dev] = true;
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) {
+        set_error("cudaFuncSetAttribute", e);
+        return FCKL_ERR_CUDA;
+      }
+      int n = di->sms / CG;
+      if (CG > 1) {
+        cfg->gridDim = dim3(static_cast<unsigned>(CG * n));
+        int m = 0;
+        if (cudaOccupancyMaxActiveClusters(&m, k, cfg) == cudaSuccess && m > 0) n = std::min(n, m);
+        cudaGetLastError();
+      }
+      max_clusters[dev] = n;
+      attr_done[dev] = true;
     }
   }
-  const int clusters = static_cast<int>(std::min<int64_t>(p.num_units, max_clusters[dev]));
+  *clusters = max_clusters[dev];
+  return FCKL_OK;
+}
+
+// Persistent launch: as many clusters as can be resident, capped by the number of work units.
+template <int BN, bool AMN, bool BMN, int EPI, bool TF32 = false>
+int launch_tc(int kind, DevInfo* di, const TcParams& p, cudaStream_t s, const char* what) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  int max_clusters = 0;
+  int st = tc_setup<BN, AMN, BMN, EPI, TF32>(di, &cfg, attr, &max_clusters);
+  if (st) return st;
+  const int clusters = static_cast<int>(std::min<int64_t>(p.num_units, max_clusters));
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG));
+  cfg.stream = s;
+  auto k = tc_gemm_kernel<CG, BN, AMN, BMN, EPI, TF32>;
   return launch(kind, s, what, [&] { cudaLaunchKernelEx(&cfg, k, p); });
 }
 
@@ -524,7 +539,7 @@ int chunk_forward(Run& r, int64_t r0, int rows, const void* Hl, bool keep = fals
   float* lse = r.lse + r0;
   float* rl = r.rl + r0;
   return launch(KIND_FWD_COMBINE, s, "fwd_combine", [&] {
-    combine_kernel<<<cblocks, 256, 0, s>>>(p.pm, p.pl, p.pc, pl.rows_alloc, pl.tiles_v, rows, p.S,
+    combine_kernel<<<cblocks, 32 * COMBINE_WARPS, 0, s>>>(p.pm, p.pl, p.pc, pl.rows_alloc, pl.tiles_v, rows, p.S,
                                            reinterpret_cast<const float*>(w + pl.off_T), wc, lse, rl);
   });
 }
@@ -1175,7 +1190,7 @@ extern "C" int fckl_forward_static(const void* H, const void* W, int dtype, cons
       return st;
     const int cblocks = static_cast<int>(cdiv(rows, 32));
     if ((st = launch(KIND_FWD_COMBINE, s, "fwd_combine", [&] {
-           combine_kernel<<<cblocks, 256, 0, s>>>(p.pm, p.pl, p.pc, pl.rows_alloc, pl.tiles_v, rows, p.S,
+           combine_kernel<<<cblocks, 32 * COMBINE_WARPS, 0, s>>>(p.pm, p.pl, p.pc, pl.rows_alloc, pl.tiles_v, rows, p.S,
                                                   reinterpret_cast<const float*>(w + pl.off_T), nullptr,
                                                   lse + r0, row_loss + r0);
          })))

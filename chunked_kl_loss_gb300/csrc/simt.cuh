@@ -73,14 +73,16 @@ __global__ void __launch_bounds__(32 * PRE_WARPS) preprocess_kernel(
 // Merge the (m, l, c) statistics of every vocabulary tile of a position:
 //   lse_n  = M + log sum_t l_t exp(m_t - M),   c_n = sum_t c_t
 //   loss_n = w_n (T_n - c_n + S_n lse_n)       (= w_n sum_k p_nk (logp_nk - z_{n,idx_nk} + lse_n))
-// with w_n = 1 when no weights are given. 32 positions per block; 8 warps split the tiles
-// and are merged in a fixed order.
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
-                                                      const float* __restrict__ pc, int ld, int tiles, int rows,
-                                                      const float* __restrict__ S, const float* __restrict__ T,
-                                                      const float* __restrict__ weight, float* __restrict__ lse_out,
-                                                      float* __restrict__ loss_out) {
-  __shared__ float sm[8][32], sl[8][32], sc[8][32];
+// with w_n = 1 when no weights are given. 32 positions per block (lane = position, so each
+// tile's statistics are read as one 128-byte line); COMBINE_WARPS warps split the tiles and are
+// merged in a fixed order, so the result does not depend on timing. Many warps per block keep
+// enough loads in flight: a chunk has only rows/32 blocks.
+constexpr int COMBINE_WARPS = 32;
+__global__ void __launch_bounds__(32 * COMBINE_WARPS) combine_kernel(
+    const float* __restrict__ pm, const float* __restrict__ pl, const float* __restrict__ pc, int ld, int tiles,
+    int rows, const float* __restrict__ S, const float* __restrict__ T, const float* __restrict__ weight,
+    float* __restrict__ lse_out, float* __restrict__ loss_out) {
+  __shared__ float sm[COMBINE_WARPS][32], sl[COMBINE_WARPS][32], sc[COMBINE_WARPS][32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int row = blockIdx.x * 32 + lane;
   const bool valid = row < rows;
@@ -88,11 +90,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   if (valid) {
     // Batches of 8 tiles: the 24 loads of a batch are issued before any of them is merged.
     constexpr int B = 8;
-    for (int t0 = w; t0 < tiles; t0 += 8 * B) {
+    for (int t0 = w; t0 < tiles; t0 += COMBINE_WARPS * B) {
       float m[B], l[B], c[B];
 #pragma unroll
       for (int b = 0; b < B; ++b) {
-        const int t = t0 + 8 * b;
+        const int t = t0 + COMBINE_WARPS * b;
         const size_t o = static_cast<size_t>(t < tiles ? t : 0) * ld + row;
         m[b] = t < tiles ? pm[o] : -INFINITY;
         l[b] = t < tiles ? pl[o] : 0.f;
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   sc[w][lane] = C;
   __syncthreads();
   if (w == 0 && valid) {
-    for (int j = 1; j < 8; ++j) {
+    for (int j = 1; j < COMBINE_WARPS; ++j) {
       const float m = sm[j][lane];
       if (m == -INFINITY) continue;
       const float nm = fmaxf(M, m);

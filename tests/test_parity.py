@@ -65,6 +65,21 @@ def test_tiny_workload_fp32(fckl):
     assert_parity(got, x, w.chunk)
 
 
+def test_two_chunks_of_1024_wide_d(fckl):
+    """Two chunks of 1024 rows (4 M-blocks each), d = 2048 (8 N-tiles), V = 8192: all of dH and
+    dW against the oracle at grad_scale 0.5, and the one call bitwise equal to the separate
+    calls."""
+    N, d, V, K, chunk = 2048, 2048, 8192, 64, 1024
+    x = synthetic.make_inputs(N, d, V, K, dtype="bf16", seed=41)
+    got = run_gpu(fckl, x, chunk, "bf16", grad_scale=0.5)
+    assert_parity(got, x, chunk, grad_scale=0.5)
+    H, W, idx, logp = to_dev(x, "bf16")
+    _, _, dH1, dW1 = fckl.forward_backward(H, W, idx, logp, chunk, grad_scale=0.5)
+    fckl.check()
+    assert np.array_equal(dH1.float().cpu().numpy().astype(np.float64), got[3])
+    assert np.array_equal(dW1.cpu().numpy().astype(np.float64), got[4])
+
+
 def test_fp32_inputs_run_tf32_logits(fckl):
     """fp32 inputs: the logits products run as tf32 on rounded copies. Against the oracle on the
     tf32-rounded inputs (what the products compute) lse and the per-position loss agree to
