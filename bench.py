@@ -379,19 +379,19 @@ def path_summary(w, api, t_ms, steps, world, prof, peak_sus, peak_src, hbm_peak=
         per_step = kn / steps
         flops_per_launch, bytes_per_launch = f_step / per_step, b_step / per_step
         t_launch = kms / kn / 1e3
-        tfl = flops_per_launch / t_launch / 1e12
-        gbs = bytes_per_launch / t_launch / 1e9
+        k_tfl = flops_per_launch / t_launch / 1e12
+        k_gbs = bytes_per_launch / t_launch / 1e9
         hbm = hbm_peak or FALLBACK["hbm_gbs"]
         tensor_bound = flops_per_launch / (peak_sus * 1e12) >= bytes_per_launch / (hbm * 1e9)
         roof = {"kernel": kname, "bound": "tensor" if tensor_bound else "hbm",
-                "achieved": tfl if tensor_bound else gbs, "peak": peak_sus if tensor_bound else hbm,
+                "achieved": k_tfl if tensor_bound else k_gbs, "peak": peak_sus if tensor_bound else hbm,
                 "unit": "TFLOP/s" if tensor_bound else "GB/s",
-                "frac": tfl / peak_sus if tensor_bound else gbs / hbm,
+                "frac": k_tfl / peak_sus if tensor_bound else k_gbs / hbm,
                 "traffic": profile_traffic(kname, w.name),
                 "peak_source": (f"{peak_src} bf16 sustained (kernel timed inside a long step)" if tensor_bound
                                 else f"{peak_src} HBM copy bandwidth"),
                 "flops_per_launch": flops_per_launch, "algorithmic_bytes_per_launch": bytes_per_launch,
-                "tensor_frac": tfl / peak_sus, "hbm_frac": gbs / hbm, "avg_launch_ms": kms / kn}
+                "tensor_frac": k_tfl / peak_sus, "hbm_frac": k_gbs / hbm, "avg_launch_ms": kms / kn}
     total = max(1e-9, sum(u[0] for u in prof.values()))
     return {"value": world * w.N * steps / (t_ms / 1e3), "ms_per_step": ms_step,
             "tflops_8NdV": tfl,

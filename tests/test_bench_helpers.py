@@ -76,3 +76,25 @@ def test_cpu_sample_is_the_first_positions_of_the_benched_inputs():
     for k in ("H", "idx", "logp"):
         assert np.array_equal(x[k][:100], full[k][:100])
     assert np.array_equal(W, full["W"])
+
+
+def test_path_summary_counts_and_kernel_roofline():
+    """The step's 8NdV count and executed FLOPs come from the step time; the roofline from the
+    dominant kernel's own launches: tensor-bound at chunk 2048, HBM-bound (dW's fp32
+    read-modify-write) at chunk 1024."""
+    for name, bound in (("n32768_d3072_v128256", "tensor"), ("n8192_d3072_v128256", "hbm")):
+        w = synthetic.WORKLOADS[name]
+        chunks = -(-w.N // w.chunk)
+        steps, t_ms = 4, 4 * 50.0
+        prof = {"bwd_dW_gemm": (steps * chunks * 1.0, steps * chunks), "fwd_logits_keep": (10.0, steps * chunks)}
+        s = bench.path_summary(w, "fused", t_ms, steps, 1, prof, 1700.0, "measured", 6700.0)
+        assert abs(s["tflops_8NdV"] - w.flops() / 0.05 / 1e12) < 1e-6 * s["tflops_8NdV"]
+        assert abs(s["tflops_executed"] - 0.75 * s["tflops_8NdV"]) < 1e-6 * s["tflops_8NdV"]
+        r = s["roofline"]
+        assert r["kernel"] == "bwd_dW_gemm" and r["bound"] == bound
+        f, b = bench.kernel_work(w, "bwd_dW_gemm")
+        assert abs(r["flops_per_launch"] - f / chunks) < 1e-3 * r["flops_per_launch"]
+        assert abs(r["tensor_frac"] - f / chunks / 1e-3 / 1e12 / 1700.0) < 1e-9
+        assert abs(r["hbm_frac"] - b / chunks / 1e-3 / 1e9 / 6700.0) < 1e-9
+        sep = bench.path_summary(w, "separate", t_ms, steps, 1, prof, 1700.0, "measured", 6700.0)
+        assert sep["tflops_executed"] == sep["tflops_8NdV"]
