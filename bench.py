@@ -529,6 +529,8 @@ def run_ours(args):
                     loss, lse = fckl.forward(b["H"], b["W"], b["idx"], b["logp"], w.chunk, ws=ws, stream=stream)
                     fckl.backward(b["H"], b["W"], b["idx"], b["logp"], lse, w.chunk, ws=ws, stream=stream, dH=dH,
                                   dW=dW)
+                if args.dp:
+                    fckl.allreduce_loss_and_dW(loss, dW)
                 freed[j].record(stream)
                 loss_host[i:i + 1].copy_(loss, non_blocking=True)
 

@@ -281,8 +281,6 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 constexpr int CG = FCKL_CG;
 constexpr int TILE_M = BM * CG;  // rows of one MMA tile
 
-// Persistent launch: one CTA (pair) per SM (pair), as many as can be resident, capped by the
-// number of work units.
 // Launch configuration of one engine instantiation: one CTA (pair) per SM (pair), as many
 // clusters as can be resident at once. The first call on a device sets the shared-memory limit
 // and asks the occupancy calculator; *clusters receives the resident cluster count.
