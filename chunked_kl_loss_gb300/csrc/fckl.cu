@@ -274,6 +274,32 @@ Plan make_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// MN-major operand staged by one copy per stage: a row-major bf16 [rows][cols] array seen as
+// 3-D (64 columns, rows, cols / 64 blocks of columns; 128-byte swizzle); a box of 64 columns x
+// BK rows x two blocks fills a stage's 2 x 8192 bytes exactly as two 2-D boxes would. Needs
+// cols % 64 == 0 (else a block would run into the next row).
+int make_map_mn3(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch_bytes) {
+  auto enc = encode_fn();
+  if (!enc) {
+    set_error_text("cuTensorMapEncodeTiled entry point not found");
+    return FCKL_ERR_CUDA;
+  }
+  cuuint64_t gdim[3] = {64, rows, cols / 64};
+  cuuint64_t gstride[2] = {pitch_bytes, 128};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BK), 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstride, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled (3-D) failed (%d): %llu x %llu",
+             static_cast<int>(r), static_cast<unsigned long long>(cols), static_cast<unsigned long long>(rows));
+    return FCKL_ERR_CUDA;
+  }
+  return FCKL_OK;
+}
+
 // ------------------------------------------------------------------ kernel launchers
 #ifndef FCKL_CG
 #define FCKL_CG 2  // CTAs per MMA in the four products: 2 = SM pairs (cta_group::2)
@@ -405,6 +431,7 @@ struct Run {
   float* dW = nullptr;
   int splits = 1;  // K-splits of the dH product
   CUtensorMap tmW_k, tmW_mn, tmDW, tmDWp;
+  int w_mn_3d = 0;  // tmW_mn is the 3-D map
 };
 
 // Clears the status word, rounds fp32 W to bf16 when needed and encodes the maps over W
@@ -436,7 +463,12 @@ int run_begin(Run& r, bool backward) {
     return st;
   }
   if (!backward) return FCKL_OK;
-  if ((st = make_map(&r.tmW_mn, r.Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, 64, BK))) return st;
+  if (CG == 2 && d % 64 == 0) {
+    if ((st = make_map_mn3(&r.tmW_mn, r.Wb, d, V, uint64_t(d) * 2))) return st;
+    r.w_mn_3d = 1;
+  } else if ((st = make_map(&r.tmW_mn, r.Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, 64, BK))) {
+    return st;
+  }
   if ((st = make_map(&r.tmDW, r.dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, V, uint64_t(d) * 4, 32, 32))) return st;
   if ((st = make_map(&r.tmDWp, r.dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, V, uint64_t(d) * 4, 256, BM,
                      CU_TENSOR_MAP_SWIZZLE_NONE)))
@@ -624,6 +656,7 @@ int chunk_backward(Run& r, int64_t r0, int rows, const void* Hl, const void* Hc,
   memset(&ph, 0, sizeof(ph));
   if ((st = make_map(&ph.tmA, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, uint64_t(pl.ldG) * 2, BK, BM))) return st;
   ph.tmB = r.tmW_mn;
+  ph.b_3d = r.w_mn_3d;
   if ((st = make_map(&ph.tmC, dhp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, uint64_t(splits) * pl.rows_alloc,
                      uint64_t(d) * 4, 32, 32)))
     return st;
@@ -656,8 +689,18 @@ int chunk_backward(Run& r, int64_t r0, int rows, const void* Hl, const void* Hc,
   // --- dW (+)= G^T H_chunk: the first chunk stores, later chunks reduce-add
   TcParams pw;
   memset(&pw, 0, sizeof(pw));
-  if ((st = make_map(&pw.tmA, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, uint64_t(pl.ldG) * 2, 64, BK))) return st;
-  if ((st = make_map(&pw.tmB, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, 64, BK))) return st;
+  if (CG == 2 && V % 64 == 0) {
+    if ((st = make_map_mn3(&pw.tmA, G, V, rows, uint64_t(pl.ldG) * 2))) return st;
+    pw.a_3d = 1;
+  } else if ((st = make_map(&pw.tmA, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, uint64_t(pl.ldG) * 2, 64, BK))) {
+    return st;
+  }
+  if (CG == 2 && d % 64 == 0) {
+    if ((st = make_map_mn3(&pw.tmB, Hc, d, rows, uint64_t(d) * 2))) return st;
+    pw.b_3d = 1;
+  } else if ((st = make_map(&pw.tmB, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, 64, BK))) {
+    return st;
+  }
   pw.tmC = r.tmDW;
   pw.tmP = r.tmDWp;
   const int kb_r = static_cast<int>(cdiv(rows, BK));

@@ -88,6 +88,9 @@ struct TcParams {
   int c_reduce;      // 1: reduce-add into tmC, 0: plain store
   int c_xlim, c_ylim;  // extent of tmC: boxes starting at or past it are not issued
   int c_prefetch;      // 1: prefetch each unit's output tile into L2 when its loads start
+  // MN-major operands: 1 when tmA / tmB is a 3-D map (64 MN-elements, K rows, 64-element MN
+  // blocks) that fetches a stage's 64-wide blocks in one copy, instead of one 2-D copy each
+  int a_3d, b_3d;
   // top-K candidate collection (teacher cache builder)
   const float* thr;  // [rows] logits at or above it are candidates
   int* cnt;          // [rows] candidates found (may exceed cmax)
@@ -348,14 +351,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             else
               tma_load_2d(dst, m, &full[s], x, y);
           };
+          // The 64-wide MN blocks of a stage sit 8192 bytes apart, as a 3-D box lays them out.
           if (!A_MN) {
             load(a, &p.tmA, kb * KE, arow);
+          } else if (CG == 2 && p.a_3d) {
+            tma_load_3d_pair(a, &p.tmA, fb, 0, kb * BK, arow / 64);
           } else {
 #pragma unroll
             for (int j = 0; j < BM / 64; ++j) load(a + j * 8192, &p.tmA, arow + 64 * j, kb * BK);
           }
           if (!B_MN) {
             load(b, &p.tmB, kb * KE, bcol);
+          } else if (CG == 2 && p.b_3d) {
+            tma_load_3d_pair(b, &p.tmB, fb, 0, kb * BK, bcol / 64);
           } else {
 #pragma unroll
             for (int j = 0; j < BN_CTA / 64; ++j) load(b + j * 8192, &p.tmB, bcol + 64 * j, kb * BK);
