@@ -79,7 +79,9 @@ typedef enum { FCKL_BF16 = 0, FCKL_F32 = 1 } fckl_dtype;
  * loss": only one chunk of positions is ever held, so memory never exceeds one chunk's size;
  * section "扩展到长上下文": peak memory grows linearly with the sequence length).
  * The size grows with chunk * V (the gradient slab) and with N only through 4 bytes per
- * position; 0 if the shape is outside the limits (including min(chunk, N) above 2^24 rows).
+ * position; for FCKL_F32 it also holds the tf32 and bf16 copies of W (6 * V * d bytes) and of
+ * one chunk of H. 0 if the shape is outside the limits (including min(chunk, N) above 2^24
+ * rows).
  * The caller allocates it; the library never does. */
 size_t fckl_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
 
