@@ -274,32 +274,6 @@ Plan make_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// MN-major operand staged by one copy per stage: a row-major bf16 [rows][cols] array seen as
-// 3-D (64 columns, rows, cols / 64 blocks of columns; 128-byte swizzle); a box of 64 columns x
-// BK rows x two blocks fills a stage's 2 x 8192 bytes exactly as two 2-D boxes would. Needs
-// cols % 64 == 0 (else a block would run into the next row).
-int make_map_mn3(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch_bytes) {
-  auto enc = encode_fn();
-  if (!enc) {
-    set_error_text("cuTensorMapEncodeTiled entry point not found");
-    return FCKL_ERR_CUDA;
-  }
-  cuuint64_t gdim[3] = {64, rows, cols / 64};
-  cuuint64_t gstride[2] = {pitch_bytes, 128};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BK), 2};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstride, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    std::lock_guard<std::mutex> lk(g_mu);
-    snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled (3-D) failed (%d): %llu x %llu",
-             static_cast<int>(r), static_cast<unsigned long long>(cols), static_cast<unsigned long long>(rows));
-    return FCKL_ERR_CUDA;
-  }
-  return FCKL_OK;
-}
-
 // ------------------------------------------------------------------ kernel launchers
 #ifndef FCKL_CG
 #define FCKL_CG 2  // CTAs per MMA in the four products: 2 = SM pairs (cta_group::2)
@@ -307,13 +281,63 @@ int make_map_mn3(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
 constexpr int CG = FCKL_CG;
 constexpr int TILE_M = BM * CG;  // rows of one MMA tile
 
+// Operand maps of the bf16 products, whose ring stages hold kps K-blocks (64 bf16 of K each):
+// two in the logits products (both operands K-major), one in dH and dW. 3-D maps fetch a whole
+// stage of an operand in one copy, laid out in shared memory as the engine expects; where the
+// needed dimension is not a multiple of 64 (or a K-major stage is one K-block) the 2-D map is
+// used and the engine issues one copy per K-block (K-major) or per 64-wide block (MN-major).
+int encode3(CUtensorMap* m, const void* base, const cuuint64_t (&gdim)[3], const cuuint64_t (&gstride)[2],
+            const cuuint32_t (&box)[3]) {
+  auto enc = encode_fn();
+  if (!enc) {
+    set_error_text("cuTensorMapEncodeTiled entry point not found");
+    return FCKL_ERR_CUDA;
+  }
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstride, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled (3-D) failed (%d): %llu x %llu x %llu",
+             static_cast<int>(r), static_cast<unsigned long long>(gdim[0]), static_cast<unsigned long long>(gdim[1]),
+             static_cast<unsigned long long>(gdim[2]));
+    return FCKL_ERR_CUDA;
+  }
+  return FCKL_OK;
+}
+
+// K-major operand, a row-major bf16 [rows][K] array read box_rows rows at a time. With two
+// K-blocks per stage and K % 64 == 0: 3-D (64 K-values, rows, K / 64 blocks), a box of
+// 64 x box_rows x 2 is a stage's two K-blocks, each rows x 128 bytes.
+int map_kmajor(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint64_t pitch_bytes, uint32_t box_rows,
+               int kps, int* is3d) {
+  *is3d = CG == 2 && kps == 2 && K % 64 == 0;
+  if (*is3d) return encode3(m, base, {64, rows, K / 64}, {pitch_bytes, 128}, {64, box_rows, 2});
+  return make_map(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, rows, pitch_bytes, BK, box_rows);
+}
+
+// MN-major operand, a row-major bf16 [K][MN] array (MN contiguous). 3-D (64 MN-values, K rows,
+// MN / 64 blocks) when MN % 64 == 0: a box of 64 x (kps * 64) x 2 is a stage of two 64-wide MN
+// blocks, kps * 8 KB apart; else 2-D boxes of 64 x (kps * 64), one per MN block.
+int map_mnmajor(CUtensorMap* m, const void* base, uint64_t MN, uint64_t K, uint64_t pitch_bytes, int kps,
+                int* is3d) {
+  *is3d = CG == 2 && MN % 64 == 0;
+  const uint32_t krows = static_cast<uint32_t>(kps * BK);
+  if (*is3d) return encode3(m, base, {64, K, MN / 64}, {pitch_bytes, 128}, {64, krows, 2});
+  return make_map(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, MN, K, pitch_bytes, 64, krows);
+}
+constexpr int KPS_LOGITS = 2;  // K-blocks per stage of the bf16 logits products
+constexpr int KPS_GRAD = 1;    // of dH and dW
+
+
 // Launch configuration of one engine instantiation: one CTA (pair) per SM (pair), as many
 // clusters as can be resident at once. The first call on a device sets the shared-memory limit
 // and asks the occupancy calculator; *clusters receives the resident cluster count.
 template <int BN, bool AMN, bool BMN, int EPI, bool TF32 = false>
 int tc_setup(DevInfo* di, cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int* clusters) {
   auto k = tc_gemm_kernel<CG, BN, AMN, BMN, EPI, TF32>;
-  constexpr uint32_t smem = TcSmem<CG, BN>::DYN_BYTES;
+  constexpr uint32_t smem = TcSmem<CG, BN, (TF32 || AMN || BMN) ? 1 : 2>::DYN_BYTES;
   static_assert(smem <= 232448, "shared memory budget");
   static bool attr_done[64] = {};  // one flag per device for this instantiation
   static int max_clusters[64] = {};
@@ -431,7 +455,7 @@ struct Run {
   float* dW = nullptr;
   int splits = 1;  // K-splits of the dH product
   CUtensorMap tmW_k, tmW_mn, tmDW, tmDWp;
-  int w_mn_3d = 0;  // tmW_mn is the 3-D map
+  int w_k_3d = 0, w_mn_3d = 0;  // tmW_k / tmW_mn are 3-D maps
 };
 
 // Clears the status word, rounds fp32 W to bf16 when needed and encodes the maps over W
@@ -458,17 +482,11 @@ int run_begin(Run& r, bool backward) {
     if ((st = make_map(&r.tmW_k, r.Wraw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, V, uint64_t(d) * 4, BK / 2,
                        VOCAB_TILE / CG)))
       return st;
-  } else if ((st = make_map(&r.tmW_k, r.Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK,
-                            VOCAB_TILE / CG))) {
+  } else if ((st = map_kmajor(&r.tmW_k, r.Wb, d, V, uint64_t(d) * 2, VOCAB_TILE / CG, KPS_LOGITS, &r.w_k_3d))) {
     return st;
   }
   if (!backward) return FCKL_OK;
-  if (CG == 2 && d % 64 == 0) {
-    if ((st = make_map_mn3(&r.tmW_mn, r.Wb, d, V, uint64_t(d) * 2))) return st;
-    r.w_mn_3d = 1;
-  } else if ((st = make_map(&r.tmW_mn, r.Wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, 64, BK))) {
-    return st;
-  }
+  if ((st = map_mnmajor(&r.tmW_mn, r.Wb, d, V, uint64_t(d) * 2, KPS_GRAD, &r.w_mn_3d))) return st;
   if ((st = make_map(&r.tmDW, r.dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, V, uint64_t(d) * 4, 32, 32))) return st;
   if ((st = make_map(&r.tmDWp, r.dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, V, uint64_t(d) * 4, 256, BM,
                      CU_TENSOR_MAP_SWIZZLE_NONE)))
@@ -512,11 +530,13 @@ int chunk_prepare(Run& r, int64_t r0, int rows, const void** Hl, const void** Hc
 }
 
 // Map of a chunk's hidden states as the logits products read them (K-major, 128 rows a box).
-int map_logits_A(const Run& r, CUtensorMap* m, const void* Hl, int rows) {
+int map_logits_A(const Run& r, CUtensorMap* m, const void* Hl, int rows, int* is3d) {
   const int d = r.pl.d;
-  if (r.dtype == FCKL_F32)
+  if (r.dtype == FCKL_F32) {
+    *is3d = 0;
     return make_map(m, Hl, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, rows, uint64_t(d) * 4, BK / 2, BM);
-  return make_map(m, Hl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM);
+  }
+  return map_kmajor(m, Hl, d, rows, uint64_t(d) * 2, BM, KPS_LOGITS, is3d);
 }
 // K-blocks of the logits products: 64 bf16 or 32 fp32 values of d per stage.
 int logits_kblocks(const Run& r) { return static_cast<int>(cdiv(r.pl.d, r.dtype == FCKL_F32 ? BK / 2 : BK)); }
@@ -530,8 +550,9 @@ int chunk_forward(Run& r, int64_t r0, int rows, const void* Hl, bool keep = fals
   int st;
   TcParams p;
   memset(&p, 0, sizeof(p));
-  if ((st = map_logits_A(r, &p.tmA, Hl, rows))) return st;
+  if ((st = map_logits_A(r, &p.tmA, Hl, rows, &p.a_3d))) return st;
   p.tmB = r.tmW_k;
+  p.b_3d = r.w_k_3d;
   const int kbl = logits_kblocks(r);
   p.sch = {static_cast<int>(cdiv(rows, TILE_M)), pl.tiles_v, kbl, 1, kbl, 1};
   p.num_units = p.sch.m_blocks * p.sch.n_blocks;
@@ -585,8 +606,9 @@ int grad_recompute(Run& r, int64_t r0, int rows, const void* Hl) {
   int st;
   TcParams pg;
   memset(&pg, 0, sizeof(pg));
-  if ((st = map_logits_A(r, &pg.tmA, Hl, rows))) return st;
+  if ((st = map_logits_A(r, &pg.tmA, Hl, rows, &pg.a_3d))) return st;
   pg.tmB = r.tmW_k;
+  pg.b_3d = r.w_k_3d;
   if ((st = make_map(&pg.tmC, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, uint64_t(pl.ldG) * 2, 64, 32)))
     return st;
   const int kbl = logits_kblocks(r);
@@ -654,7 +676,7 @@ int chunk_backward(Run& r, int64_t r0, int rows, const void* Hl, const void* Hc,
   const int splits = r.splits;
   TcParams ph;
   memset(&ph, 0, sizeof(ph));
-  if ((st = make_map(&ph.tmA, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, uint64_t(pl.ldG) * 2, BK, BM))) return st;
+  if ((st = map_kmajor(&ph.tmA, G, V, rows, uint64_t(pl.ldG) * 2, BM, KPS_GRAD, &ph.a_3d))) return st;
   ph.tmB = r.tmW_mn;
   ph.b_3d = r.w_mn_3d;
   if ((st = make_map(&ph.tmC, dhp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, uint64_t(splits) * pl.rows_alloc,
@@ -689,18 +711,8 @@ int chunk_backward(Run& r, int64_t r0, int rows, const void* Hl, const void* Hc,
   // --- dW (+)= G^T H_chunk: the first chunk stores, later chunks reduce-add
   TcParams pw;
   memset(&pw, 0, sizeof(pw));
-  if (CG == 2 && V % 64 == 0) {
-    if ((st = make_map_mn3(&pw.tmA, G, V, rows, uint64_t(pl.ldG) * 2))) return st;
-    pw.a_3d = 1;
-  } else if ((st = make_map(&pw.tmA, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, rows, uint64_t(pl.ldG) * 2, 64, BK))) {
-    return st;
-  }
-  if (CG == 2 && d % 64 == 0) {
-    if ((st = make_map_mn3(&pw.tmB, Hc, d, rows, uint64_t(d) * 2))) return st;
-    pw.b_3d = 1;
-  } else if ((st = make_map(&pw.tmB, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, 64, BK))) {
-    return st;
-  }
+  if ((st = map_mnmajor(&pw.tmA, G, V, rows, uint64_t(pl.ldG) * 2, KPS_GRAD, &pw.a_3d))) return st;
+  if ((st = map_mnmajor(&pw.tmB, Hc, d, rows, uint64_t(d) * 2, KPS_GRAD, &pw.b_3d))) return st;
   pw.tmC = r.tmDW;
   pw.tmP = r.tmDWp;
   const int kb_r = static_cast<int>(cdiv(rows, BK));
@@ -941,7 +953,12 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
     Wl = w + tp.off_Wt;
   }
   CUtensorMap tmW;
-  if ((st = make_map(&tmW, Wl, mdt, d, V, uint64_t(d) * esz, ke, VOCAB_TILE / CG))) return st;
+  int w3d = 0;
+  if (f32) {
+    if ((st = make_map(&tmW, Wl, mdt, d, V, uint64_t(d) * esz, ke, VOCAB_TILE / CG))) return st;
+  } else if ((st = map_kmajor(&tmW, Wl, d, V, uint64_t(d) * 2, VOCAB_TILE / CG, KPS_LOGITS, &w3d))) {
+    return st;
+  }
   float* pm = reinterpret_cast<float*>(w + tp.off_pm);
   float* pl = reinterpret_cast<float*>(w + tp.off_pl);
   float* lse = reinterpret_cast<float*>(w + tp.off_lse);
@@ -961,8 +978,13 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
     // pass 1: per (row, vocabulary tile) max and sum-exp
     TcParams p;
     memset(&p, 0, sizeof(p));
-    if ((st = make_map(&p.tmA, Hc, mdt, d, rows, uint64_t(d) * esz, ke, BM))) return st;
+    if (f32) {
+      if ((st = make_map(&p.tmA, Hc, mdt, d, rows, uint64_t(d) * esz, ke, BM))) return st;
+    } else if ((st = map_kmajor(&p.tmA, Hc, d, rows, uint64_t(d) * 2, BM, KPS_LOGITS, &p.a_3d))) {
+      return st;
+    }
     p.tmB = tmW;
+    p.b_3d = w3d;
     p.sch = {static_cast<int>(cdiv(rows, TILE_M)), tp.tiles_v, kbl, 1, kbl, 1};
     p.num_units = p.sch.m_blocks * p.sch.n_blocks;
     p.status = status;
@@ -1204,15 +1226,17 @@ extern "C" int fckl_forward_static(const void* H, const void* W, int dtype, cons
     return FCKL_ERR_CUDA;
   }
   CUtensorMap tmW;
-  if ((st = make_map(&tmW, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, V, uint64_t(d) * 2, BK, VOCAB_TILE / CG))) return st;
+  int w3d = 0;
+  if ((st = map_kmajor(&tmW, W, d, V, uint64_t(d) * 2, VOCAB_TILE / CG, KPS_LOGITS, &w3d))) return st;
   for (int64_t r0 = 0; r0 < N; r0 += pl.chunk) {
     const int rows = static_cast<int>(std::min<int64_t>(pl.chunk, N - r0));
     if ((st = launch_preprocess(pl, idx + r0 * K, logp + r0 * K, rows, w, dstatus, di, s))) return st;
     const void* Hc = static_cast<const uint8_t*>(H) + static_cast<size_t>(r0) * d * 2;
     TcParams p;
     memset(&p, 0, sizeof(p));
-    if ((st = make_map(&p.tmA, Hc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, rows, uint64_t(d) * 2, BK, BM))) return st;
+    if ((st = map_kmajor(&p.tmA, Hc, d, rows, uint64_t(d) * 2, BM, KPS_LOGITS, &p.a_3d))) return st;
     p.tmB = tmW;
+    p.b_3d = w3d;
     p.sch = {static_cast<int>(cdiv(rows, TILE_M)), pl.tiles_v, static_cast<int>(cdiv(d, BK)), 1,
              static_cast<int>(cdiv(d, BK)), 1};
     p.num_units = p.sch.m_blocks * p.sch.n_blocks;

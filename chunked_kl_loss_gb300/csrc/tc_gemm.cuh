@@ -3,8 +3,9 @@
 // One CTA per SM, 192 threads. With CG = 2 two SMs of a cluster form a pair that computes a
 // 256 x BN tile with tcgen05.mma.cta_group::2: each CTA stages its 128 rows of A and half of
 // B, the even CTA issues the MMAs, and each CTA's TMEM receives its 128 rows of the result
-// (CG = 1: one CTA per 128 x BN tile). K-blocks of 64 bf16.
-//   warp 0     : TMA producer (one lane) filling a shared-memory ring (6 stages for pairs)
+// (CG = 1: one CTA per 128 x BN tile). K-blocks of 64 bf16 (32 fp32), two per ring stage in
+// the bf16 logits products.
+//   warp 0     : TMA producer (one lane) filling a shared-memory ring (192 KB per CTA for pairs)
 //   warp 1     : TMEM owner and, in the even CTA, MMA issuer (one lane); two TMEM
 //                accumulators of 128 x 256 fp32 per CTA so the epilogue of one tile
 //                overlaps the main loop of the next
@@ -88,9 +89,10 @@ struct TcParams {
   int c_reduce;      // 1: reduce-add into tmC, 0: plain store
   int c_xlim, c_ylim;  // extent of tmC: boxes starting at or past it are not issued
   int c_prefetch;      // 1: prefetch each unit's output tile into L2 when its loads start
-  // MN-major operands: 1 when tmA / tmB is a 3-D map (64 MN-elements, K rows, 64-element MN
-  // blocks) that fetches a stage's 64-wide blocks in one copy, instead of one 2-D copy each
-  int a_3d, b_3d;
+  // 1 when tmA / tmB is a 3-D map that fetches a whole stage of the operand in one copy: for an
+  // MN-major operand (64 MN-values, K rows, 64-wide MN blocks), instead of one 2-D copy per block;
+  int a_3d, b_3d;  // (bf16 products, two K-blocks per stage) also for K-major operands: one 3-D
+                   // copy (64 K-values, rows, K-blocks) fetches a stage's two K-blocks
   // top-K candidate collection (teacher cache builder)
   const float* thr;  // [rows] logits at or above it are candidates
   int* cnt;          // [rows] candidates found (may exceed cmax)
@@ -100,13 +102,17 @@ struct TcParams {
 };
 
 // Shared-memory layout of one CTA. CG = CTAs per MMA (1: a 128 x BN tile per CTA; 2: a
-// 256 x BN tile per CTA pair, each CTA holding its 128 rows of A and BN/2 rows of B).
-template <int CG, int BN>
+// 256 x BN tile per CTA pair, each CTA holding its 128 rows of A and BN/2 rows of B). A ring
+// stage holds KPS K-blocks (128 bytes of K per row each): the same bytes in flight in fewer,
+// larger stages, so that the per-stage hand-off (barriers, commit, copies) is paid less often.
+template <int CG, int BN, int KPS>
 struct TcSmem {
-  static constexpr int STAGES = CG == 2 ? 6 : 4;
+  static constexpr int STAGES = (CG == 2 ? 6 : 4) / KPS;
   static constexpr int BN_CTA = BN / CG;
-  static constexpr uint32_t A_BYTES = BM * BK * 2;
-  static constexpr uint32_t B_BYTES = BN_CTA * BK * 2;
+  static constexpr uint32_t A_KB = BM * BK * 2;      // one K-block of A
+  static constexpr uint32_t B_KB = BN_CTA * BK * 2;  // one K-block of B
+  static constexpr uint32_t A_BYTES = KPS * A_KB;
+  static constexpr uint32_t B_BYTES = KPS * B_KB;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t EPI_OFF = STAGES * STAGE_BYTES;
   static constexpr uint32_t BAR_OFF = EPI_OFF + EPI_WARPS * 2 * EPI_BUF_BYTES;
@@ -260,10 +266,14 @@ __device__ __forceinline__ bool wait_phase_cluster(uint64_t* bar, uint32_t parit
 // same descriptors as 64 bf16 values, with four MMAs of K = 8 instead of K = 16.
 template <int CG, int BN, bool A_MN, bool B_MN, int EPI, bool TF32 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-  using L = TcSmem<CG, BN>;
+  // K-blocks per ring stage: two for the bf16 products with both operands K-major (the logits
+  // products), where the larger stages measured 4-6% faster; one for dH and dW, where they did
+  // not help (dW, both operands MN-major, was 6% slower).
+  constexpr int KPS = (TF32 || A_MN || B_MN) ? 1 : 2;
+  using L = TcSmem<CG, BN, KPS>;
   constexpr int NST = L::STAGES;
   constexpr int BN_CTA = L::BN_CTA;
-  constexpr int KE = TF32 ? BK / 2 : BK;  // K elements per stage (128 bytes of each row)
+  constexpr int KE = TF32 ? BK / 2 : BK;  // K elements per K-block (128 bytes of each row)
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per MMA");
   static_assert(!B_MN || BN_CTA % 64 == 0, "MN-major B is staged in 64-wide blocks");
   static_assert(!TF32 || (!A_MN && !B_MN), "tf32 operands are staged K-major");
@@ -331,7 +341,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         // a whole main loop before the epilogue needs it.
         if (EPI == EPI_STORE_F32 && p.c_prefetch && nb * BN < p.c_xlim && arow < p.c_ylim)
           tma_prefetch_l2_2d(&p.tmP, nb * BN, arow);
-        for (int kb = kb0; kb < kb1; ++kb, ++cnt) {
+        for (int kb = kb0; kb < kb1; kb += KPS, ++cnt) {
           const uint32_t s = cnt % NST, ph = (cnt / NST) & 1u;
           if (!wait_phase(&empty[s], ph ^ 1u, abort_flag, p.status)) {
             ok = false;
@@ -351,22 +361,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             else
               tma_load_2d(dst, m, &full[s], x, y);
           };
-          // The 64-wide MN blocks of a stage sit 8192 bytes apart, as a 3-D box lays them out.
+          // Stage layouts, as the 3-D boxes lay them out. K-major: K-block j of the stage at
+          // j * A_KB (rows x 128 bytes). MN-major: the 64-wide MN block i at i * KPS * 8192, its
+          // KPS * 64 K rows in order, so K-block j starts j * 8192 bytes into each block. A copy
+          // past the unit's K range (an odd count) or past K lands data the MMAs skip or zeros.
           if (!A_MN) {
-            load(a, &p.tmA, kb * KE, arow);
+            if (!TF32 && CG == 2 && p.a_3d) {
+              tma_load_3d_pair(a, &p.tmA, fb, 0, arow, kb);
+            } else {
+#pragma unroll
+              for (int j = 0; j < KPS; ++j) load(a + j * L::A_KB, &p.tmA, (kb + j) * KE, arow);
+            }
           } else if (CG == 2 && p.a_3d) {
             tma_load_3d_pair(a, &p.tmA, fb, 0, kb * BK, arow / 64);
           } else {
 #pragma unroll
-            for (int j = 0; j < BM / 64; ++j) load(a + j * 8192, &p.tmA, arow + 64 * j, kb * BK);
+            for (int i = 0; i < BM / 64; ++i) load(a + i * KPS * 8192, &p.tmA, arow + 64 * i, kb * BK);
           }
           if (!B_MN) {
-            load(b, &p.tmB, kb * KE, bcol);
+            if (!TF32 && CG == 2 && p.b_3d) {
+              tma_load_3d_pair(b, &p.tmB, fb, 0, bcol, kb);
+            } else {
+#pragma unroll
+              for (int j = 0; j < KPS; ++j) load(b + j * L::B_KB, &p.tmB, (kb + j) * KE, bcol);
+            }
           } else if (CG == 2 && p.b_3d) {
             tma_load_3d_pair(b, &p.tmB, fb, 0, kb * BK, bcol / 64);
           } else {
 #pragma unroll
-            for (int j = 0; j < BN_CTA / 64; ++j) load(b + j * 8192, &p.tmB, bcol + 64 * j, kb * BK);
+            for (int i = 0; i < BN_CTA / 64; ++i) load(b + i * KPS * 8192, &p.tmB, bcol + 64 * i, kb * BK);
           }
         }
       }
@@ -397,7 +420,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         if (!got) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
-        for (int kb = kb0; kb < kb1; ++kb, ++cnt) {
+        for (int kb = kb0; kb < kb1; kb += KPS, ++cnt) {
           const uint32_t s = cnt % NST, ph = (cnt / NST) & 1u;
           if (!wait_phase(&full[s], ph, abort_flag, p.status)) {
             ok = false;
@@ -407,12 +430,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           const uint32_t a_addr = smem_u32(smem + s * L::STAGE_BYTES);
           const uint32_t b_addr = a_addr + L::A_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = A_MN ? make_sdesc_sw128(a_addr + kk * 2048, 8192, 1024)
-                                     : make_sdesc_sw128(a_addr + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? make_sdesc_sw128(b_addr + kk * 2048, 8192, 1024)
-                                     : make_sdesc_sw128(b_addr + kk * 32, 16, 1024);
-            const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
+          for (int q = 0; q < KPS * (BK / 16); ++q) {
+            const int j = q / (BK / 16), kk = q % (BK / 16);  // K-block of the stage, K step in it
+            if (KPS > 1 && kb + j >= kb1) break;               // past the unit's K range
+            const uint64_t ad = A_MN ? make_sdesc_sw128(a_addr + j * 8192 + kk * 2048, KPS * 8192, 1024)
+                                     : make_sdesc_sw128(a_addr + j * L::A_KB + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? make_sdesc_sw128(b_addr + j * 8192 + kk * 2048, KPS * 8192, 1024)
+                                     : make_sdesc_sw128(b_addr + j * L::B_KB + kk * 32, 16, 1024);
+            const uint32_t accum = (kb > kb0 || q > 0) ? 1u : 0u;
             if constexpr (CG == 2 && TF32)
               umma_tf32_pair(d_tmem, ad, bd, IDESC, accum);
             else if constexpr (CG == 2)
