@@ -167,6 +167,9 @@ def config_of(w, api="fused", dp_world=0):
             "input_dtype": w.dtype, "parallelism": par, "api": api,
             "logits": ("kept by the forward (fp16 exp(z - tile max) in the gradient slab)" if api == "fused"
                        else "recomputed in the backward"),
+            "workspace": ("overlap (fckl_overlap_workspace_bytes): each chunk's G pass runs on a second stream "
+                          "beside the next chunk's forward" if api == "fused"
+                          else "the first fckl_workspace_bytes of the same workspace (chunks in sequence)"),
             "l2": "inputs larger than L2 (W alone is %.0f MB)" % (w.V * w.d * 2 / 1e6)}
 
 
@@ -400,7 +403,11 @@ def path_summary(w, api, t_ms, steps, world, prof, peak_sus, peak_src, hbm_peak=
             "tflops_executed": tfl_exec, "tflops_executed_frac_of_sustained": tfl_exec / peak_sus,
             "roofline": roof,
             "kernel_shares": {k: round(v[0] / total, 4) for k, v in prof.items() if v[1]},
-            "kernel_ms_per_step": sum(v[0] for v in prof.values()) / steps}
+            "kernel_ms_per_step": sum(v[0] for v in prof.values()) / steps,
+            "kernel_shares_note": ("shares of the summed per-kernel event time" + (
+                "; the G pass (bwd_grad_from_logits) runs on a second stream beside the next chunk's forward, "
+                "so the summed time exceeds the step and both kernels' event times include the overlap"
+                if api == "fused" else ""))}
 
 
 def replica_seed(seed, rank):
@@ -433,7 +440,9 @@ def run_ours(args):
     base_alloc = torch.cuda.memory_allocated(dev)
     H, W, idx, logp = (host[k].to(dev) for k in ("H", "W", "idx", "logp"))
     dt = fckl.BF16 if w.dtype == "bf16" else fckl.F32
-    ws = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, dt, dev)
+    # the one call overlaps consecutive chunks with this workspace; the separate calls use
+    # its first part (fckl_workspace_bytes)
+    ws = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, dt, dev, kind="loss_overlap")
     dH = torch.empty_like(H)
     dW = torch.empty(w.V, w.d, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -615,14 +624,14 @@ def memory_sweep(args):
     W = torch.from_numpy(x["W"]).to(dev).to(torch.bfloat16)
     idx_h, logp_h = torch.from_numpy(x["idx"]), torch.from_numpy(x["logp"])
     del x
-    def peak_of(n, fused):
+    def peak_of(n, fused, kind="loss"):
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
         base = torch.cuda.memory_allocated(dev)  # W already resident
         torch.cuda.reset_peak_memory_stats(dev)
         H = Hh[:n].to(dev)
         idx, logp = idx_h[:n].to(dev), logp_h[:n].to(dev)
-        ws = fckl.Workspace(n, w.d, w.V, w.K, w.chunk, fckl.BF16, dev)
+        ws = fckl.Workspace(n, w.d, w.V, w.K, w.chunk, fckl.BF16, dev, kind=kind)
         if fused:
             fckl.forward_backward(H, W, idx, logp, w.chunk, ws=ws)
         else:
@@ -642,9 +651,13 @@ def memory_sweep(args):
     sizes = (w.N // 8, w.N // 4, w.N // 2, w.N)
     sep = fit([(n, peak_of(n, False)) for n in sizes])
     fused = fit([(n, peak_of(n, True)) for n in sizes])
+    overlap = fit([(n, peak_of(n, True, "loss_overlap")) for n in sizes])
+    second_set = (fckl.overlap_workspace_bytes(w.N, w.d, w.V, w.K, w.chunk, fckl.BF16)
+                  - fckl.workspace_bytes(w.N, w.d, w.V, w.K, w.chunk, fckl.BF16))
     line = {"metric": "peak device memory of one forward+backward vs N (GiB)", "workload": w.name,
             "chunk": w.chunk, "analytic_bytes_per_position": bytes_per_position(w),
-            "separate_calls": sep, "one_call": fused}
+            "separate_calls": sep, "one_call": fused, "one_call_overlap": overlap,
+            "second_buffer_set_gib": second_set / 2**30}
     print(json.dumps(line), flush=True)
     return line
 

@@ -22,7 +22,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["LIB_PATH", "FcklError", "load", "workspace_bytes", "Workspace", "forward", "backward",
+__all__ = ["LIB_PATH", "FcklError", "load", "workspace_bytes", "overlap_workspace_bytes", "Workspace", "forward", "backward",
            "forward_backward", "fused_chunked_kl", "teacher_topk", "check", "shard_range",
            "allreduce_loss_and_dW", "data_parallel_forward_backward", "launch_count", "profile_enable", "profile_read",
            "kernel_names", "OK", "ERR_ARG", "ERR_INDEX", "ERR_CUDA", "ERR_TIMEOUT",
@@ -58,6 +58,8 @@ def load():
     vp, i64, i32, sz, f32 = c.c_void_p, c.c_int64, c.c_int, c.c_size_t, c.c_float
     lib.fckl_workspace_bytes.restype = sz
     lib.fckl_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
+    lib.fckl_overlap_workspace_bytes.restype = sz
+    lib.fckl_overlap_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
     lib.fckl_forward.restype = i32
     lib.fckl_forward.argtypes = [vp, vp, i32, vp, vp, vp, i64, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
     lib.fckl_backward.restype = i32
@@ -114,10 +116,16 @@ def workspace_bytes(N: int, d: int, V: int, K: int, chunk: int, dtype: int = BF1
     return int(load().fckl_workspace_bytes(N, d, V, K, chunk, dtype))
 
 
+def overlap_workspace_bytes(N: int, d: int, V: int, K: int, chunk: int, dtype: int = BF16) -> int:
+    return int(load().fckl_overlap_workspace_bytes(N, d, V, K, chunk, dtype))
+
+
 class Workspace:
     """A device workspace sized for one problem shape (a torch uint8 tensor); ``kind`` is
-    "loss" (forward, backward, forward_backward), "topk" (teacher cache builder keeping each
-    chunk's logits) or "topk_min" (the builder's minimum, which projects each chunk twice)."""
+    "loss" (forward, backward, forward_backward), "loss_overlap" (the same, plus a second set
+    of one chunk's buffers with which forward_backward overlaps consecutive chunks), "topk"
+    (teacher cache builder keeping each chunk's logits) or "topk_min" (the builder's minimum,
+    which projects each chunk twice)."""
 
     def __init__(self, N, d, V, K, chunk, dtype=BF16, device=None, kind="loss"):
         import torch
@@ -127,6 +135,8 @@ class Workspace:
             n = int(load().fckl_topk_workspace_bytes(N, d, V, K, chunk, dtype))
         elif kind == "loss":
             n = workspace_bytes(N, d, V, K, chunk, dtype)
+        elif kind == "loss_overlap":
+            n = overlap_workspace_bytes(N, d, V, K, chunk, dtype)
         else:
             raise ValueError(f"unknown workspace kind {kind!r}")
         if n == 0:
@@ -169,11 +179,11 @@ def _shape(H, W, idx, logp):
     return N, d, V, K
 
 
-def _ws_for(ws, N, d, V, K, chunk, dt, device):
+def _ws_for(ws, N, d, V, K, chunk, dt, device, kind="loss"):
     global _last_ws
     import weakref
     if ws is None:
-        ws = Workspace(N, d, V, K, chunk, dt, device)
+        ws = Workspace(N, d, V, K, chunk, dt, device, kind=kind)
         _last_ws = ws
     else:
         _last_ws = weakref.ref(ws)
@@ -222,12 +232,14 @@ def forward_backward(H, W, idx, logp, chunk, grad_scale=1.0, ws=None, stream=Non
     """(loss, lse, dH, dW) — or (loss, lse, row_loss, dH, dW) with ``row_loss=True`` — from
     one fckl_forward_backward call: each chunk's backward right after its forward, from what
     the forward kept in the gradient slab (no logits recomputed). Bitwise the outputs of
-    forward() then backward()."""
+    forward() then backward(). Without ``ws`` it allocates the "loss_overlap" workspace, with
+    which consecutive chunks overlap (one more chunk's buffers); pass a "loss" workspace for
+    the minimum memory."""
     import torch
     N, d, V, K = _shape(H, W, idx, logp)
     weight = _weight(weight, N)
     dt = _dtype_code(H)
-    ws = _ws_for(ws, N, d, V, K, chunk, dt, H.device)
+    ws = _ws_for(ws, N, d, V, K, chunk, dt, H.device, kind="loss_overlap")
     loss = torch.empty(1, dtype=torch.float32, device=H.device)
     lse = torch.empty(N, dtype=torch.float32, device=H.device)
     rl = torch.empty(N, dtype=torch.float32, device=H.device) if row_loss else None

@@ -215,7 +215,27 @@ struct Plan {
   int bn_d;        // N-tile of the dH / dW products
   size_t off_status, off_sidx, off_sp, off_S, off_T, off_pm, off_pl, off_pc, off_rowloss, off_G, off_dhp,
       off_Hb, off_Wb, off_Ht, off_Wt, total;
+  // A second set of the per-chunk buffers (ordered slots, S, T, tile statistics, gradient slab,
+  // bf16 H copy), after everything above; present when there is more than one chunk. With it
+  // (a workspace of total_overlap bytes) the one call forms chunk c's G on a second stream
+  // while chunk c+1's forward runs.
+  size_t alt_sidx, alt_sp, alt_S, alt_T, alt_pm, alt_pl, alt_pc, alt_G, alt_Hb, total_overlap;
 };
+
+// The plan as seen by a chunk in buffer set 1: the same layout with the second set's offsets.
+Plan second_set(const Plan& p) {
+  Plan q = p;
+  q.off_sidx = p.alt_sidx;
+  q.off_sp = p.alt_sp;
+  q.off_S = p.alt_S;
+  q.off_T = p.alt_T;
+  q.off_pm = p.alt_pm;
+  q.off_pl = p.alt_pl;
+  q.off_pc = p.alt_pc;
+  q.off_G = p.alt_G;
+  q.off_Hb = p.alt_Hb;
+  return q;
+}
 
 // N-tile of the dH and dW products (over d). 256 columns: an SM pair stages 128 each, two
 // 64-wide swizzle blocks; a d that is not a multiple of 256 ends in a ragged tile.
@@ -269,6 +289,18 @@ Plan make_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
   p.off_Ht = dt == FCKL_F32 ? take(R * d * 4) : o;
   p.off_Wt = dt == FCKL_F32 ? take(static_cast<size_t>(V) * d * 4) : o;
   p.total = o;
+  if (N > p.chunk) {
+    p.alt_sidx = take(R * K * 4);
+    p.alt_sp = take(R * K * 4);
+    p.alt_S = take(R * 4);
+    p.alt_T = take(R * 4);
+    p.alt_pm = take(static_cast<size_t>(p.tiles_v) * R * 4);
+    p.alt_pl = take(static_cast<size_t>(p.tiles_v) * R * 4);
+    p.alt_pc = take(static_cast<size_t>(p.tiles_v) * R * 4);
+    p.alt_G = take(R * p.ldG * 2);
+    p.alt_Hb = dt == FCKL_F32 ? take(R * d * 2) : o;
+  }
+  p.total_overlap = o;
   return p;
 }
 
@@ -436,7 +468,9 @@ int common_checks(const void* H, const void* W, int dt, const int32_t* idx, cons
 
 // Everything one call needs to run the per-chunk steps.
 struct Run {
-  Plan pl;
+  Plan pl;   // buffer set 0
+  Plan pl1;  // buffer set 1 (second_set(pl)), used by the overlapped one call
+  const Plan& plan(int set) const { return set ? pl1 : pl; }
   DevInfo* di = nullptr;
   cudaStream_t s = nullptr;
   uint8_t* w = nullptr;  // workspace
@@ -512,8 +546,8 @@ int run_begin(Run& r, bool backward) {
 // Orders the chunk's cache slots; returns the chunk's H rows as the logits products read them
 // (*Hl: bf16, or for fp32 inputs a tf32-rounded copy) and as the dW product reads them (*Hc:
 // bf16; for fp32 inputs a bf16 copy, made only when `backward`).
-int chunk_prepare(Run& r, int64_t r0, int rows, const void** Hl, const void** Hc, bool backward) {
-  const Plan& pl = r.pl;
+int chunk_prepare(Run& r, int set, int64_t r0, int rows, const void** Hl, const void** Hc, bool backward) {
+  const Plan& pl = r.plan(set);
   int st = launch_preprocess(pl, r.idx + r0 * pl.K, r.logp + r0 * pl.K, rows, r.w, r.status, r.di, r.s);
   if (st) return st;
   const size_t esz = r.dtype == FCKL_F32 ? 4 : 2;
@@ -544,8 +578,8 @@ int logits_kblocks(const Run& r) { return static_cast<int>(cdiv(r.pl.d, r.dtype 
 // Forward of one chunk: logits tiles -> per-tile (max, sum-exp, gathered sum) -> lse and loss.
 // With keep, exp(z - tile max) is also stored (fp16) into the gradient slab for the chunk's
 // backward.
-int chunk_forward(Run& r, int64_t r0, int rows, const void* Hl, bool keep = false) {
-  const Plan& pl = r.pl;
+int chunk_forward(Run& r, int set, int64_t r0, int rows, const void* Hl, bool keep = false) {
+  const Plan& pl = r.plan(set);
   uint8_t* w = r.w;
   int st;
   TcParams p;
@@ -596,8 +630,8 @@ int chunk_forward(Run& r, int64_t r0, int rows, const void* Hl, bool keep = fals
 }
 
 // G = scale * w_n * (S softmax(z) - p_sparse) of one chunk, from its recomputed logits.
-int grad_recompute(Run& r, int64_t r0, int rows, const void* Hl) {
-  const Plan& pl = r.pl;
+int grad_recompute(Run& r, int set, int64_t r0, int rows, const void* Hl) {
+  const Plan& pl = r.plan(set);
   const int V = pl.V;
   uint8_t* w = r.w;
   cudaStream_t s = r.s;
@@ -631,15 +665,18 @@ int grad_recompute(Run& r, int64_t r0, int rows, const void* Hl) {
   return launch_tc<VOCAB_TILE, false, false, EPI_LOGIT_GRAD>(KIND_BWD_GRAD, r.di, pg, s, "bwd_logit_grad");
 }
 
+constexpr int GRAD_BLOCKS_PER_SM = 8;  // blocks per SM of the G pass when it runs alone
+
 // The same G formed in place from what the chunk's forward kept in the slab (fp16
-// exp(z - tile max), with the tile maxima in pm).
-int grad_from_kept(Run& r, int64_t r0, int rows) {
-  const Plan& pl = r.pl;
+// exp(z - tile max), with the tile maxima in pm), on stream s: alone (GRAD_BLOCKS_PER_SM blocks
+// per SM) or, with beside, one block per SM next to a tensor-core product.
+int grad_from_kept(Run& r, int set, int64_t r0, int rows, cudaStream_t s, bool beside) {
+  const Plan& pl = r.plan(set);
   const int V = pl.V;
   uint8_t* w = r.w;
-  cudaStream_t s = r.s;
   const int64_t units = int64_t(rows) * cdiv(V, KG_SEG);
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(units, int64_t(r.di->sms) * 8)));
+  const int grid =
+      static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(units, int64_t(r.di->sms) * (beside ? 1 : GRAD_BLOCKS_PER_SM))));
   __nv_bfloat16* G = reinterpret_cast<__nv_bfloat16*>(w + pl.off_G);
   const int* sidx = reinterpret_cast<const int*>(w + pl.off_sidx);
   const float* spp = reinterpret_cast<const float*>(w + pl.off_sp);
@@ -650,15 +687,31 @@ int grad_from_kept(Run& r, int64_t r0, int rows) {
   const float gsc = r.grad_scale;
   const int K = pl.K, ldp = pl.rows_alloc;
   const int64_t ld = pl.ldG;
+  if (beside) {
+    static bool done[64] = {};
+    std::lock_guard<std::mutex> lk(g_setup_mu);
+    if (!done[r.di->id]) {
+      cudaError_t e = cudaFuncSetAttribute(logit_grad_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) {
+        set_error("cudaFuncSetAttribute(logit_grad_kernel)", e);
+        return FCKL_ERR_CUDA;
+      }
+      done[r.di->id] = true;
+    }
+  }
   return launch(KIND_BWD_GRAD_KEPT, s, "bwd_grad_from_logits", [&] {
-    logit_grad_kernel<<<grid, GRAD_THREADS, 0, s>>>(G, ld, rows, V, K, sidx, spp, S, lse, wr, gsc, pm, ldp);
+    if (beside)
+      logit_grad_kernel<true><<<grid, GRAD_THREADS, 0, s>>>(G, ld, rows, V, K, sidx, spp, S, lse, wr, gsc, pm, ldp);
+    else
+      logit_grad_kernel<false><<<grid, GRAD_THREADS, 0, s>>>(G, ld, rows, V, K, sidx, spp, S, lse, wr, gsc, pm, ldp);
   });
 }
 
-// Backward of one chunk: G from recomputed logits (or, with keep, from what the chunk's forward
-// kept in the slab), then dH_chunk = G W and dW (+)= G^T H_chunk.
-int chunk_backward(Run& r, int64_t r0, int rows, const void* Hl, const void* Hc, bool keep = false) {
-  const Plan& pl = r.pl;
+// The gradient products of one chunk whose G is in its slab: dH_chunk = G W and
+// dW (+)= G^T H_chunk.
+int chunk_products(Run& r, int set, int64_t r0, int rows, const void* Hc) {
+  const Plan& pl = r.plan(set);
   const int d = pl.d, V = pl.V;
   uint8_t* w = r.w;
   cudaStream_t s = r.s;
@@ -667,9 +720,6 @@ int chunk_backward(Run& r, int64_t r0, int rows, const void* Hl, const void* Hc,
   const int mbr = static_cast<int>(cdiv(rows, TILE_M));
   const int kb_v = static_cast<int>(cdiv(V, BK));
   int st;
-
-  // --- G = scale * w_n * (S softmax(z) - p_sparse), z kept or recomputed
-  if ((st = keep ? grad_from_kept(r, r0, rows) : grad_recompute(r, r0, rows, Hl))) return st;
 
   // --- dH_chunk = G W, split over the vocabulary into fp32 partials, then summed
   const int nbd = static_cast<int>(cdiv(d, pl.bn_d));
@@ -725,6 +775,93 @@ int chunk_backward(Run& r, int64_t r0, int rows, const void* Hl, const void* Hc,
   pw.c_xlim = d;
   pw.c_ylim = V;
   return launch_tc<256, true, true, EPI_STORE_F32>(KIND_BWD_DW, r.di, pw, s, "bwd_dW_gemm");
+}
+
+// Backward of one chunk: G = scale * w_n * (S softmax(z) - p_sparse) from recomputed logits
+// (or, with keep, from what the chunk's forward kept in the slab), then the gradient products.
+int chunk_backward(Run& r, int set, int64_t r0, int rows, const void* Hl, const void* Hc, bool keep = false) {
+  int st = keep ? grad_from_kept(r, set, r0, rows, r.s, false) : grad_recompute(r, set, r0, rows, Hl);
+  if (st) return st;
+  return chunk_products(r, set, r0, rows, Hc);
+}
+
+// Second stream of the one call and its fork/join events, one set per host thread and device
+// (calls from different host threads never share them), created on first use and kept.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+thread_local SideStream t_side[64];
+
+int side_stream(int dev, SideStream** out) {
+  SideStream& x = t_side[dev];
+  if (!x.s) {
+    SideStream n;
+    cudaError_t e = cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      set_error("side stream set-up", e);
+      if (n.join) cudaEventDestroy(n.join);
+      if (n.fork) cudaEventDestroy(n.fork);
+      if (n.s) cudaStreamDestroy(n.s);
+      return FCKL_ERR_CUDA;
+    }
+    x = n;
+  }
+  *out = &x;
+  return FCKL_OK;
+}
+
+// The one call over chunks c = 0, 1, ... with chunk c in buffer set c % 2: after chunk c's
+// forward and chunk c+1's preprocessing, chunk c's G is formed on the second stream (one
+// block per SM, which fits beside a tensor-core product's CTA) while chunk c+1's forward runs
+// on the caller's stream; the caller's stream then waits for G before chunk c's gradient
+// products. The last chunk's G runs on the caller's stream. Every kernel computes what it
+// does in the sequential order from the same inputs, so the results are bitwise the same.
+// The HBM-bound G pass thus runs under a tensor-bound product instead of between two.
+int run_overlapped(Run& r, SideStream* side) {
+  const int64_t N = r.pl.N, C = r.pl.chunk;
+  int64_t r0 = 0;
+  int rows = static_cast<int>(std::min<int64_t>(C, N));
+  const void *Hl = nullptr, *Hc = nullptr;
+  int st;
+  if ((st = chunk_prepare(r, 0, r0, rows, &Hl, &Hc, true))) return st;
+  if ((st = chunk_forward(r, 0, r0, rows, Hl, true))) return st;
+  for (int set = 0;; set ^= 1) {
+    const int64_t n0 = r0 + C;
+    if (n0 >= N) {
+      if ((st = grad_from_kept(r, set, r0, rows, r.s, false))) return st;
+      return chunk_products(r, set, r0, rows, Hc);
+    }
+    const int nrows = static_cast<int>(std::min<int64_t>(C, N - n0));
+    const void *nHl = nullptr, *nHc = nullptr;
+    // G waits for the next chunk's preprocessing too, so that it is released together with
+    // that chunk's forward rather than ahead of it
+    if ((st = chunk_prepare(r, set ^ 1, n0, nrows, &nHl, &nHc, true))) return st;
+    cudaError_t e = cudaEventRecord(side->fork, r.s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->s, side->fork, 0);
+    if (e != cudaSuccess) {
+      set_error("fork to the side stream", e);
+      return FCKL_ERR_CUDA;
+    }
+    st = grad_from_kept(r, set, r0, rows, side->s, true);
+    // the join is recorded and waited for even after a failed launch, so that nothing of
+    // this call is left running outside the caller's stream
+    e = cudaEventRecord(side->join, side->s);
+    if (!st) st = chunk_forward(r, set ^ 1, n0, nrows, nHl, true);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(r.s, side->join, 0);
+    if (e != cudaSuccess) {
+      set_error("join from the side stream", e);
+      return FCKL_ERR_CUDA;
+    }
+    if (st) return st;
+    if ((st = chunk_products(r, set, r0, rows, Hc))) return st;
+    r0 = n0;
+    rows = nrows;
+    Hl = nHl;
+    Hc = nHc;
+  }
 }
 
 int run_loss(Run& r, float* loss) {
@@ -815,6 +952,11 @@ size_t fckl_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype
   return make_plan(N, d, V, K, chunk, dtype).total;
 }
 
+size_t fckl_overlap_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype) {
+  if (check_shape(N, d, V, K, chunk, dtype) != FCKL_OK) return 0;
+  return make_plan(N, d, V, K, chunk, dtype).total_overlap;
+}
+
 
 int fckl_forward(const void* H, const void* W, int dtype, const int32_t* idx, const float* logp,
                  const float* weight, int64_t N, int d, int V, int K, int chunk, float* loss, float* lse,
@@ -829,8 +971,8 @@ int fckl_forward(const void* H, const void* W, int dtype, const int32_t* idx, co
   for (int64_t r0 = 0; r0 < N; r0 += r.pl.chunk) {
     const int rows = static_cast<int>(std::min<int64_t>(r.pl.chunk, N - r0));
     const void *Hl = nullptr, *Hc = nullptr;
-    if ((st = chunk_prepare(r, r0, rows, &Hl, &Hc, false))) return st;
-    if ((st = chunk_forward(r, r0, rows, Hl))) return st;
+    if ((st = chunk_prepare(r, 0, r0, rows, &Hl, &Hc, false))) return st;
+    if ((st = chunk_forward(r, 0, r0, rows, Hl))) return st;
   }
   return run_loss(r, loss);
 }
@@ -850,8 +992,8 @@ int fckl_backward(const void* H, const void* W, int dtype, const int32_t* idx, c
   for (int64_t r0 = 0; r0 < N; r0 += r.pl.chunk) {
     const int rows = static_cast<int>(std::min<int64_t>(r.pl.chunk, N - r0));
     const void *Hl = nullptr, *Hc = nullptr;
-    if ((st = chunk_prepare(r, r0, rows, &Hl, &Hc, true))) return st;
-    if ((st = chunk_backward(r, r0, rows, Hl, Hc))) return st;
+    if ((st = chunk_prepare(r, 0, r0, rows, &Hl, &Hc, true))) return st;
+    if ((st = chunk_backward(r, 0, r0, rows, Hl, Hc))) return st;
   }
   return FCKL_OK;
 }
@@ -871,13 +1013,24 @@ int fckl_forward_backward(const void* H, const void* W, int dtype, const int32_t
   r.grad_scale = grad_scale;
   r.dH = dH;
   r.dW = dW;
+  // With the second buffer set in the workspace, G of each chunk overlaps the next forward.
+  const bool overlap = N > r.pl.chunk && ws_bytes >= r.pl.total_overlap;
+  SideStream* side = nullptr;
+  if (overlap) {
+    r.pl1 = second_set(r.pl);
+    if ((st = side_stream(r.di->id, &side))) return st;
+  }
   if ((st = run_begin(r, true))) return st;
+  if (overlap) {
+    if ((st = run_overlapped(r, side))) return st;
+    return run_loss(r, loss);
+  }
   for (int64_t r0 = 0; r0 < N; r0 += r.pl.chunk) {
     const int rows = static_cast<int>(std::min<int64_t>(r.pl.chunk, N - r0));
     const void *Hl = nullptr, *Hc = nullptr;
-    if ((st = chunk_prepare(r, r0, rows, &Hl, &Hc, true))) return st;
-    if ((st = chunk_forward(r, r0, rows, Hl, true))) return st;
-    if ((st = chunk_backward(r, r0, rows, Hl, Hc, true))) return st;
+    if ((st = chunk_prepare(r, 0, r0, rows, &Hl, &Hc, true))) return st;
+    if ((st = chunk_forward(r, 0, r0, rows, Hl, true))) return st;
+    if ((st = chunk_backward(r, 0, r0, rows, Hl, Hc, true))) return st;
   }
   return run_loss(r, loss);
 }

@@ -389,22 +389,25 @@ __global__ void __launch_bounds__(256) dh_reduce_kernel(const float* __restrict_
 // position and KG_SEG columns, each thread takes 16 adjacent columns per step (two 16-byte
 // loads and stores at the same addresses), GRAD_STEPS steps 4096 columns apart, all loads
 // issued before the arithmetic (128 bytes in flight per thread), together with the steps' tile
-// maxima and the row's scalars. The row's ordered cache slots sit in shared memory (two
-// buffers, alternating by unit, so one barrier per unit suffices) and each thread walks them
-// with one cursor. Row pitch ld is a multiple of 8 elements; columns in [V, ld) are written as 0.
+// maxima and the row's scalars. Each thread walks the row's ordered cache slots with one
+// cursor, read through L1 (no shared memory: a block then fits on an SM beside a tensor-core
+// product that holds nearly all of it, so this pass can run concurrently with one). Row pitch
+// ld is a multiple of 8 elements; columns in [V, ld) are written as 0.
 constexpr int KG_COLS = 16;
 constexpr int KG_SEG = GRAD_THREADS * KG_COLS * GRAD_STEPS;
 
+// BESIDE = true: the same code as a separate function, launched beside a tensor-core product
+// and set to prefer the largest shared-memory carve-out, so that an SM it lands on first stays
+// configured for that product's CTAs; BESIDE = false keeps the default carve-out (more L1 for
+// loads in flight) for the pass that runs alone.
+template <bool BESIDE>
 __global__ void __launch_bounds__(GRAD_THREADS) logit_grad_kernel(
     __nv_bfloat16* __restrict__ G, int64_t ld, int rows, int V, int K, const int* __restrict__ sidx,
     const float* __restrict__ sp, const float* __restrict__ S, const float* __restrict__ lse,
     const float* __restrict__ wrow, float gscale, const float* __restrict__ pm, int ld_part) {
-  __shared__ int s_ids[2][K_LIMIT];  // two units' slots: one barrier per unit suffices
-  __shared__ float s_p[2][K_LIMIT];
   const int segs = (V + KG_SEG - 1) / KG_SEG;
   const int64_t units = static_cast<int64_t>(rows) * segs;
-  int par = 0;
-  for (int64_t u = blockIdx.x; u < units; u += gridDim.x, par ^= 1) {
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
     const int row = static_cast<int>(u / segs);
     const int seg = static_cast<int>(u - static_cast<int64_t>(row) * segs);
     __nv_bfloat16* gr = G + static_cast<int64_t>(row) * ld;
@@ -422,20 +425,15 @@ __global__ void __launch_bounds__(GRAD_THREADS) logit_grad_kernel(
     }
     const float wv = wrow ? __ldg(wrow + row) : 1.f;
     const float sv = __ldg(S + row), lv = __ldg(lse + row);
-    int* ids = s_ids[par];
-    float* pv = s_p[par];
-    for (int k = threadIdx.x; k < K; k += GRAD_THREADS) {
-      ids[k] = __ldg(sidx + static_cast<int64_t>(row) * K + k);
-      pv[k] = __ldg(sp + static_cast<int64_t>(row) * K + k);
-    }
-    __syncthreads();
+    const int* ids = sidx + static_cast<int64_t>(row) * K;
+    const float* pv = sp + static_cast<int64_t>(row) * K;
     const float gs = __fmul_rn(gscale, wv);
     const float a = __fmul_rn(gs, sv);
     const float nl = __fmul_rn(-lv, LOG2E);
     int lo = 0, hi = K;  // cursor: first slot whose id is >= c0
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
-      if (ids[mid] < c0)
+      if (__ldg(ids + mid) < c0)
         lo = mid + 1;
       else
         hi = mid;
@@ -450,10 +448,10 @@ __global__ void __launch_bounds__(GRAD_THREADS) logit_grad_kernel(
       float x[KG_COLS];
 #pragma unroll
       for (int t = 0; t < KG_COLS; ++t) x[t] = grad_dense(f, eh[t]);
-      while (k < K && ids[k] < c) ++k;
-      while (k < K && ids[k] < c + KG_COLS) {
-        const int pos = ids[k] - c;
-        const float v = __fmul_rn(gs, pv[k]);
+      while (k < K && __ldg(ids + k) < c) ++k;
+      while (k < K && __ldg(ids + k) < c + KG_COLS) {
+        const int pos = __ldg(ids + k) - c;
+        const float v = __fmul_rn(gs, __ldg(pv + k));
 #pragma unroll
         for (int t = 0; t < KG_COLS; ++t) x[t] = (t == pos) ? __fsub_rn(x[t], v) : x[t];
         ++k;

@@ -85,6 +85,17 @@ typedef enum { FCKL_BF16 = 0, FCKL_F32 = 1 } fckl_dtype;
  * The caller allocates it; the library never does. */
 size_t fckl_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
 
+/* Bytes of a workspace with which fckl_forward_backward overlaps the steps of consecutive
+ * chunks (same citation: at most two chunks' buffers are held, still independent of N beyond
+ * the 4 bytes per position). With N > chunk this adds a second set of one chunk's buffers
+ * (gradient slab, chunk * V * 2 bytes, and the chunk's ordered cache slots and tile
+ * statistics) to fckl_workspace_bytes(); each chunk's G is then formed on a library-owned
+ * second stream while the next chunk's forward runs on the caller's stream, and the caller's
+ * stream waits for it before that chunk's gradient products, so the call still completes in
+ * the caller's stream order and its results are bitwise those of the smaller workspace. With
+ * N <= chunk it equals fckl_workspace_bytes(). 0 if the shape is outside the limits. */
+size_t fckl_overlap_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
+
 /* Forward pass ("Hugging Face：让知识蒸馏廉价到可大规模运行", paragraph "Fused, chunked KL
  * loss": each chunk's hidden states are projected to logits, folded into the accumulated loss
  * and dropped before the next chunk; paragraph "离线蒸馏": the loss is taken against the cached

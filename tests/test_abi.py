@@ -65,6 +65,25 @@ def test_workspace_size_rules(fckl):
         rows = -(-min(chunk, N) // 256) * 256
         tiles = -(-V // 256)
         assert 0 <= extra - rows * (-(-V // 8) * 8) * 4 - rows * tiles * 4 - rows * 4 < 3072
+    # the overlap workspace: a second set of one chunk's buffers (ordered slots and their
+    # masses, S and T, the three tile-statistics arrays, the gradient slab and, for fp32 inputs,
+    # the chunk's bf16 H copy; 1 KiB rounding each) when there is more than one chunk
+    ov = fckl.overlap_workspace_bytes
+    for N, d, V, K, chunk, dt in [(32768, 3072, 128256, 100, 2048, fckl.BF16), (130, 320, 2057, 100, 100, fckl.BF16),
+                                  (300, 256, 4096, 16, 64, fckl.F32)]:
+        rows = -(-min(chunk, N) // 256) * 256
+        tiles = -(-V // 256)
+        want = 2 * rows * K * 4 + 2 * rows * 4 + 3 * tiles * rows * 4 + rows * (-(-V // 8) * 8) * 2
+        regions = 8
+        if dt == fckl.F32:
+            want += rows * d * 2
+            regions += 1
+        extra = ov(N, d, V, K, chunk, dt) - ws(N, d, V, K, chunk, dt)
+        assert 0 <= extra - want < regions * 1024, (extra, want)
+    assert ov(2048, 256, 4096, 16, 2048, fckl.BF16) == ws(2048, 256, 4096, 16, 2048, fckl.BF16) > 0  # one chunk
+    assert ov(2048, 256, 4096, 16, 4096, fckl.BF16) == ws(2048, 256, 4096, 16, 4096, fckl.BF16)
+    assert ov(2049, 256, 4096, 16, 2048, fckl.BF16) > ws(2049, 256, 4096, 16, 2048, fckl.BF16)
+    assert ov(0, 256, 4096, 16, 16, fckl.BF16) == 0 and ov(64, 250, 4096, 16, 16, fckl.BF16) == 0
     # outside the limits: 0
     assert ws(0, 256, 4096, 16, 16, fckl.BF16) == 0
     assert ws(64, 250, 4096, 16, 16, fckl.BF16) == 0  # d % 8 != 0

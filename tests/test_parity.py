@@ -311,14 +311,16 @@ def test_bounded_wait_times_out_and_context_survives(fckl):
     assert_parity(got, x, 64)
 
 
-def test_two_streams_two_workspaces(fckl):
+@pytest.mark.parametrize("kind", ["loss", "loss_overlap"])
+def test_two_streams_two_workspaces(fckl, kind):
     """Calls on two streams with their own workspaces do not interfere: the library keeps no
-    device state between calls, so interleaved calls give the bits of sequential ones."""
+    device state between calls, so interleaved calls give the bits of sequential ones (with
+    the overlap workspace both calls also share this host thread's second stream)."""
     xa = synthetic.make_inputs(260, 256, 3000, 20, dtype="bf16", seed=31)
     xb = synthetic.make_inputs(200, 128, 2500, 10, dtype="bf16", seed=32)
     ta, tb = to_dev(xa, "bf16"), to_dev(xb, "bf16")
-    wa = fckl.Workspace(260, 256, 3000, 20, 128, fckl.BF16)
-    wb = fckl.Workspace(200, 128, 2500, 10, 64, fckl.BF16)
+    wa = fckl.Workspace(260, 256, 3000, 20, 128, fckl.BF16, kind=kind)
+    wb = fckl.Workspace(200, 128, 2500, 10, 64, fckl.BF16, kind=kind)
     ref_a = fckl.forward_backward(*ta, 128, ws=wa)
     ref_b = fckl.forward_backward(*tb, 64, ws=wb)
     torch.cuda.synchronize()
@@ -385,10 +387,12 @@ def test_one_call_captured_in_a_cuda_graph(fckl):
     assert not torch.equal(ref_b[0], ref_a[0])
 
 
-def test_calls_from_two_host_threads(fckl):
+@pytest.mark.parametrize("kind", ["loss", "loss_overlap"])
+def test_calls_from_two_host_threads(fckl, kind):
     """Two host threads call the one call at the same time, each on its own stream and
     workspace (ctypes releases the interpreter lock during the call, so the library's host code
-    runs concurrently): the results are those of sequential calls, bit for bit."""
+    runs concurrently): the results are those of sequential calls, bit for bit (with the
+    overlap workspace each thread forks to its own second stream)."""
     import threading
     xa = synthetic.make_inputs(300, 256, 3000, 20, dtype="bf16", seed=71)
     xb = synthetic.make_inputs(200, 128, 2500, 10, dtype="bf16", seed=72)
@@ -402,7 +406,8 @@ def test_calls_from_two_host_threads(fckl):
         try:
             torch.cuda.set_device(0)
             s = torch.cuda.Stream()
-            ws = fckl.Workspace(t[0].shape[0], t[0].shape[1], t[1].shape[0], t[2].shape[1], chunk, fckl.BF16)
+            ws = fckl.Workspace(t[0].shape[0], t[0].shape[1], t[1].shape[0], t[2].shape[1], chunk, fckl.BF16,
+                                kind=kind)
             outs = []
             with torch.cuda.stream(s):
                 for _ in range(seq):
