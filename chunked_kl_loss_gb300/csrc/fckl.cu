@@ -785,17 +785,47 @@ int chunk_backward(Run& r, int set, int64_t r0, int rows, const void* Hl, const 
   return chunk_products(r, set, r0, rows, Hc);
 }
 
+// Id of the current CUDA context, unique within the process (a device reset, or another
+// context of the device, gets a new one); 0 if it cannot be read.
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, &id) == CUDA_SUCCESS)
+    return id;
+  return 0;
+}
+
 // Second stream of the one call and its fork/join events, one set per host thread and device
-// (calls from different host threads never share them), created on first use and kept.
+// (calls from different host threads never share them), created on first use and kept for the
+// context they were made in: under a new context of the device (after a device reset) a new
+// set is made (the old handles belong to the destroyed context and are not touched).
 struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
+  unsigned long long ctx = 0;
 };
 thread_local SideStream t_side[64];
 
 int side_stream(int dev, SideStream** out) {
   SideStream& x = t_side[dev];
-  if (!x.s) {
+  const unsigned long long id = current_context_id();
+  if (!x.s || (id != 0 && id != x.ctx)) {
     SideStream n;
     cudaError_t e = cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming);
@@ -807,6 +837,7 @@ int side_stream(int dev, SideStream** out) {
       if (n.s) cudaStreamDestroy(n.s);
       return FCKL_ERR_CUDA;
     }
+    n.ctx = current_context_id();  // read after the creation, which makes the context current
     x = n;
   }
   *out = &x;
