@@ -1,6 +1,7 @@
 """GPU parity at the full workload sizes, in the launch configuration bench.py times (one
-fckl_forward_backward call per step: the workload's chunk, every chunk's forward, G pass, dH
-product and dW reduce-add, the same dH split).
+fckl_forward_backward call per step with the overlap workspace: the workload's chunk, every
+chunk's forward, G pass (beside the next chunk's forward on the second stream), dH product and
+dW reduce-add, the same dH split).
 
 The oracle cannot redo a whole workload inside a test, so each workload is checked three ways:
 
@@ -16,8 +17,9 @@ The oracle cannot redo a whole workload inside a test, so each workload is check
   exactly: the weighted loss, every dH row (the zero-weight rows must be exactly 0) and all of
   dW [V, d], element by element. Every chunk's reduce-add into dW contributes to what is
   compared.
-* At the headline size, the separate forward and backward calls (logits recomputed) give the
-  same bits as the one call.
+* At the headline size, the separate forward and backward calls (logits recomputed) and the
+  one call with the minimum workspace (chunks in sequence) give the same bits as the
+  overlapped one call.
 
 The pages state that the dense, forward-chunked and fused variants compute the same loss
 ("Hugging Face：让知识蒸馏廉价到可大规模运行", paragraph "Fused, chunked KL loss"); these
@@ -91,7 +93,7 @@ def test_full_size_against_oracle(fckl, name):
     logp = torch.from_numpy(x["logp"]).to(dev)
     Hq = synthetic.round_bf16(x["H"])  # the values the device sees, widened exactly
     Wq = synthetic.round_bf16(x["W"])
-    ws = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, fckl.BF16)
+    ws = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, fckl.BF16, kind="loss_overlap")
 
     # ---- unweighted run: sampled positions, golden total loss, properties
     loss, lse, rl, dH, dW = fckl.forward_backward(H, W, idx, logp, w.chunk, ws=ws, row_loss=True)
@@ -100,6 +102,10 @@ def test_full_size_against_oracle(fckl, name):
         ws2 = fckl.Workspace(w.N, w.d, w.V, w.K, w.chunk, fckl.BF16)
         loss2, lse2, rl2 = fckl.forward(H, W, idx, logp, w.chunk, ws=ws2, row_loss=True)
         dH2, dW2 = fckl.backward(H, W, idx, logp, lse2, w.chunk, ws=ws2)
+        assert fckl.check(ws2) == fckl.OK
+        for a, b in ((loss, loss2), (lse, lse2), (rl, rl2), (dH, dH2), (dW, dW2)):
+            assert torch.equal(a, b)
+        loss2, lse2, rl2, dH2, dW2 = fckl.forward_backward(H, W, idx, logp, w.chunk, ws=ws2, row_loss=True)
         assert fckl.check(ws2) == fckl.OK
         for a, b in ((loss, loss2), (lse, lse2), (rl, rl2), (dH, dH2), (dW, dW2)):
             assert torch.equal(a, b)
