@@ -18,6 +18,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -539,6 +540,13 @@ int run_begin(Run& r, bool backward) {
       best = eff;
       r.splits = sp;
     }
+  }
+  // FCKL_SPLITS (environment, 1..MAX_SPLITS) overrides the count for tuning; a count whose
+  // K-blocks would leave a split empty is ignored. Results then differ from the default only
+  // by the fp32 summation order of the partials.
+  if (const char* env = std::getenv("FCKL_SPLITS")) {
+    const int sp = std::atoi(env);
+    if (sp >= 1 && sp <= MAX_SPLITS && sp <= kb_v && cdiv(kb_v, cdiv(kb_v, sp)) == sp) r.splits = sp;
   }
   return FCKL_OK;
 }

@@ -428,3 +428,26 @@ def test_calls_from_two_host_threads(fckl, kind):
         for o in outs:
             for u, v in zip(o, ref):
                 assert torch.equal(u, v)
+
+
+def test_dH_split_count_override(fckl, monkeypatch):
+    """FCKL_SPLITS sets the number of K-splits of dH = G W (1..4). Only dH's fp32 summation order
+    changes: loss, lse and dW are bitwise the default's, dH stays within the oracle tolerance;
+    values outside 1..4 (or not numbers) are ignored."""
+    N, d, V, K, chunk = 600, 256, 5000, 40, 128
+    x = synthetic.make_inputs(N, d, V, K, dtype="bf16", seed=81)
+    t = to_dev(x, "bf16")
+    monkeypatch.delenv("FCKL_SPLITS", raising=False)
+    ref = [u.clone() for u in fckl.forward_backward(*t, chunk)]
+    fckl.check()
+    r_dH, _ = orc.backward(x["H"], x["W"], x["idx"], x["logp"], 1.0, chunk)
+    for val in ("1", "2", "3", "4", "9", "0", "abc"):
+        monkeypatch.setenv("FCKL_SPLITS", val)
+        got = fckl.forward_backward(*t, chunk)
+        fckl.check()
+        for i in (0, 1, 3):  # loss, lse, dW
+            assert torch.equal(got[i], ref[i]), (val, i)
+        g = got[2].float().cpu().numpy().astype(np.float64)
+        assert np.abs(g - r_dH).max() <= GRAD_TOL * np.abs(r_dH).max(), val
+        if val in ("9", "0", "abc"):
+            assert torch.equal(got[2], ref[2]), val
