@@ -700,6 +700,8 @@ def topk_bench(args):
     products = 1 if keep else 2
     cfg = config_of(w, "teacher_topk")
     cfg["logits"] = "kept from pass 1" if keep else "projected again in pass 2"
+    cfg["workspace"] = ("fckl_topk_kept_logits_workspace_bytes: the chunk's fp32 logits kept for pass 2" if keep
+                        else "fckl_topk_workspace_bytes: the minimum, logits projected twice")
     line = {"metric": "teacher top-K cache build positions/s", "value": w.N / (ms / 1e3),
             "unit": UNIT, "ms_per_step": ms, "steps": args.steps, "warmup": args.warmup,
             "tflops_executed": 2.0 * products * w.N * w.d * w.V / (ms / 1e3) / 1e12, "dtype": "bf16",
