@@ -51,6 +51,10 @@ def one_call(fckl, t, chunk, kind, dt, weight=None, grad_scale=1.0):
     (2048, 512, 8192, 64, 1024, "bf16"),  # two full chunks of 4 M-blocks
     (1100, 64, 300, 5, 100, "bf16"),      # 11 chunks, V below two vocabulary tiles
     (100, 64, 1000, 8, 100, "bf16"),      # one chunk: no second set, the same workspace
+    (5, 64, 300, 5, 1, "bf16"),           # five one-row chunks: the buffer sets alternate every row
+    (33, 8, 100, 100, 16, "bf16"),        # d = 8, V below one tile, K = V; last chunk one row
+    (257, 128, 2049, 1024, 128, "bf16"),  # K = 1024 slots; last chunk one row; V % 8 = 1
+    (700, 264, 3000, 30, 300, "f32"),     # fp32, d not a multiple of 64, ragged chunks of 300
 ])
 def test_overlap_is_bitwise_the_sequential_one_call(fckl, N, d, V, K, chunk, dtype):
     x = synthetic.make_inputs(N, d, V, K, dtype=dtype, seed=N + 7 * V)
