@@ -16,14 +16,16 @@
  * a chunk, folds it into the running loss and drops it; the backward pass recomputes
  * the chunk's logits to form G (the one-call path instead keeps, in the gradient slab itself,
  * what its backward needs of the chunk's logits, see fckl_forward_backward). Only one chunk x V
- * slab is ever held.
+ * slab is ever held (two with the workspace of fckl_overlap_workspace_bytes).
  *
  * Conventions for every call below
  *  - All arrays are dense and row-major. "device" pointers are CUDA device memory of the
  *    current device; the caller owns every buffer, including the workspace. The library
  *    allocates no device memory at run time (the one exception is the fixed scratch array
  *    of fckl_forward_static, reserved when the library is loaded) and keeps only host-side
- *    caches (device properties, one-time kernel set-up).
+ *    caches (device properties, one-time kernel set-up) and, for fckl_forward_backward with
+ *    the overlap workspace, one non-blocking CUDA stream and two events per host thread and
+ *    device, created on first use and kept.
  *  - H is [N, d] and W is [V, d], both of type `dtype` (FCKL_BF16 or FCKL_F32). With FCKL_F32
  *    the logits products (the forward projection, the backward's recompute, both passes of
  *    the top-K builder) run on the tensor cores as tf32 with fp32 accumulation, on copies of
@@ -144,7 +146,10 @@ int fckl_backward(const void* H, const void* W, int dtype,
  * operations (tile maximum, fp16 e, the same products and roundings), so the two calls give
  * bitwise identical outputs. Not an operation of the pages' method: their backward recomputes
  * each chunk only because their forward drops it ("Fused, chunked KL loss"); here the backward
- * directly follows the forward. */
+ * directly follows the forward. With ws_bytes >= fckl_overlap_workspace_bytes() and N > chunk,
+ * consecutive chunks overlap: chunk c's G pass runs on the library's second stream beside chunk
+ * c+1's forward, joined back into `stream` before chunk c's gradient products and before the
+ * call returns; the outputs are bitwise those of the smaller workspace. */
 int fckl_forward_backward(const void* H, const void* W, int dtype,
                           const int32_t* idx, const float* logp, const float* weight,
                           int64_t N, int d, int V, int K, int chunk, float grad_scale,
