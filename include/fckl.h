@@ -137,7 +137,8 @@ int fckl_backward(const void* H, const void* W, int dtype,
 /* Forward and backward in one call, chunk by chunk: each chunk's backward runs right after
  * its forward (lse_n depends on position n alone), so the chunk's cache slots are ordered
  * once and its hidden states are re-read while still in L2. Outputs as fckl_forward and
- * fckl_backward (row_loss may be NULL); same workspace size.
+ * fckl_backward (row_loss may be NULL); the same workspace as the separate calls, or the
+ * larger one of fckl_overlap_workspace_bytes (below).
  * The chunk's logits are not recomputed: its forward stores e = exp(z - m) as fp16 into the
  * gradient slab (m: the logit's 256-column tile maximum, kept with the softmax statistics)
  * and its backward turns the slab into G in place, G = S_n exp(m - lse_n) e - p at the cached
