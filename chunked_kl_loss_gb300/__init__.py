@@ -73,6 +73,8 @@ def load():
     lib.fckl_topk_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
     lib.fckl_topk_kept_logits_workspace_bytes.restype = sz
     lib.fckl_topk_kept_logits_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
+    lib.fckl_topk_overlap_workspace_bytes.restype = sz
+    lib.fckl_topk_overlap_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
     lib.fckl_teacher_topk.restype = i32
     lib.fckl_teacher_topk.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, vp, vp, vp, sz, vp]
     lib.fckl_check.restype = i32
@@ -124,13 +126,16 @@ class Workspace:
     """A device workspace sized for one problem shape (a torch uint8 tensor); ``kind`` is
     "loss" (forward, backward, forward_backward), "loss_overlap" (the same, plus a second set
     of one chunk's buffers with which forward_backward overlaps consecutive chunks), "topk"
-    (teacher cache builder keeping each chunk's logits) or "topk_min" (the builder's minimum,
-    which projects each chunk twice)."""
+    (teacher cache builder keeping each chunk's logits), "topk_overlap" (the same plus a second
+    set of one chunk's buffers, with which the builder overlaps consecutive chunks) or
+    "topk_min" (the builder's minimum, which projects each chunk twice)."""
 
     def __init__(self, N, d, V, K, chunk, dtype=BF16, device=None, kind="loss"):
         import torch
         if kind == "topk":
             n = int(load().fckl_topk_kept_logits_workspace_bytes(N, d, V, K, chunk, dtype))
+        elif kind == "topk_overlap":
+            n = int(load().fckl_topk_overlap_workspace_bytes(N, d, V, K, chunk, dtype))
         elif kind == "topk_min":
             n = int(load().fckl_topk_workspace_bytes(N, d, V, K, chunk, dtype))
         elif kind == "loss":
@@ -364,7 +369,8 @@ def teacher_topk(Ht, Wt, K, chunk, ws=None, stream=None, keep_logits=True):
     """Offline teacher cache: (idx int32 [N, K], logp fp32 [N, K]) — the K tokens of largest
     teacher logit per position, by logit descending, with full-softmax log-probabilities.
     ``keep_logits=False`` hands the library only the minimum workspace, so it projects each
-    chunk twice instead of keeping its logits; the outputs are the same."""
+    chunk twice instead of keeping its logits; the outputs are the same. Without ``ws`` the
+    "topk_overlap" workspace is allocated (consecutive chunks overlap)."""
     import torch
     N, d = Ht.shape
     V = Wt.shape[0]
@@ -377,7 +383,7 @@ def teacher_topk(Ht, Wt, K, chunk, ws=None, stream=None, keep_logits=True):
     global _last_ws
     import weakref
     if ws is None:
-        ws = Workspace(N, d, V, K, chunk, dt, Ht.device, kind="topk" if keep_logits else "topk_min")
+        ws = Workspace(N, d, V, K, chunk, dt, Ht.device, kind="topk_overlap" if keep_logits else "topk_min")
         _last_ws = ws
     else:
         _last_ws = weakref.ref(ws)

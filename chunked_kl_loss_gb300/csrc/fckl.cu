@@ -826,6 +826,7 @@ unsigned long long current_context_id() {
 struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t join_set[2] = {nullptr, nullptr};  // the side work of each buffer set (top-K builder)
   unsigned long long ctx = 0;
 };
 thread_local SideStream t_side[64];
@@ -838,8 +839,12 @@ int side_stream(int dev, SideStream** out) {
     cudaError_t e = cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.join_set[0], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.join_set[1], cudaEventDisableTiming);
     if (e != cudaSuccess) {
       set_error("side stream set-up", e);
+      for (cudaEvent_t ev : n.join_set)
+        if (ev) cudaEventDestroy(ev);
       if (n.join) cudaEventDestroy(n.join);
       if (n.fork) cudaEventDestroy(n.fork);
       if (n.s) cudaStreamDestroy(n.s);
@@ -849,6 +854,16 @@ int side_stream(int dev, SideStream** out) {
     x = n;
   }
   *out = &x;
+  return FCKL_OK;
+}
+
+// Makes stream s wait for event ev (stream order only, no host wait).
+int wait_event(cudaStream_t s, cudaEvent_t ev) {
+  const cudaError_t e = cudaStreamWaitEvent(s, ev, 0);
+  if (e != cudaSuccess) {
+    set_error("join from the side stream", e);
+    return FCKL_ERR_CUDA;
+  }
   return FCKL_OK;
 }
 
@@ -941,6 +956,11 @@ struct TopkPlan {
   // the chunk's fp32 logits from pass 1, read by the collect step, and per position the list
   // of tiles whose maximum reaches the threshold
   size_t off_Z, off_live, off_live_cnt, total_keep;
+  // A second set of what pass 2 and the selection of a chunk use (lse, threshold, counts,
+  // candidates, kept logits, live-tile lists), after everything above when there is more than
+  // one chunk: with it (total_overlap bytes) chunk c's collect and select run on a second
+  // stream beside chunk c+1's pass 1.
+  size_t alt_lse, alt_thr, alt_cnt, alt_cv, alt_cz, alt_Z, alt_live, alt_live_cnt, total_overlap;
 };
 
 TopkPlan make_topk_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
@@ -976,6 +996,17 @@ TopkPlan make_topk_plan(int64_t N, int d, int V, int K, int chunk, int dt) {
   p.off_live = take(R * static_cast<size_t>(p.tiles_v) * 4);
   p.off_live_cnt = take(R * 4);
   p.total_keep = o;
+  if (N > p.chunk) {
+    p.alt_lse = take(R * 4);
+    p.alt_thr = take(R * 4);
+    p.alt_cnt = take(R * 4);
+    p.alt_cv = take(R * p.cmax * 4);
+    p.alt_cz = take(R * p.cmax * 4);
+    p.alt_Z = take(R * p.ldz * 4);
+    p.alt_live = take(R * static_cast<size_t>(p.tiles_v) * 4);
+    p.alt_live_cnt = take(R * 4);
+  }
+  p.total_overlap = o;
   return p;
 }
 
@@ -1100,6 +1131,11 @@ size_t fckl_topk_kept_logits_workspace_bytes(int64_t N, int d, int V, int K, int
   return make_topk_plan(N, d, V, K, chunk, dtype).total_keep;
 }
 
+size_t fckl_topk_overlap_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype) {
+  if (check_shape(N, d, V, K, chunk, dtype) != FCKL_OK) return 0;
+  return make_topk_plan(N, d, V, K, chunk, dtype).total_overlap;
+}
+
 int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int d, int V, int K, int chunk,
                       int32_t* idx, float* logp, void* ws, size_t ws_bytes, void* stream) {
   int st = check_shape(N, d, V, K, chunk, dtype);
@@ -1153,13 +1189,52 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
   }
   float* pm = reinterpret_cast<float*>(w + tp.off_pm);
   float* pl = reinterpret_cast<float*>(w + tp.off_pl);
-  float* lse = reinterpret_cast<float*>(w + tp.off_lse);
-  float* thr = reinterpret_cast<float*>(w + tp.off_thr);
-  int* cnt = reinterpret_cast<int*>(w + tp.off_cnt);
-  int* cv = reinterpret_cast<int*>(w + tp.off_cv);
-  float* cz = reinterpret_cast<float*>(w + tp.off_cz);
+  // Buffers of the chunk's pass 2 and selection, per buffer set (chunk c uses set c % 2 when
+  // the workspace holds the second set; then chunk c's collect and select run on the side
+  // stream beside chunk c+1's pass 1).
+  struct Set {
+    float *lse, *thr, *cz, *Z;
+    int *cnt, *cv, *live, *live_cnt;
+  } sets[2];
+  auto set_at = [&](size_t olse, size_t othr, size_t ocnt, size_t ocv, size_t ocz, size_t oZ, size_t olive,
+                    size_t olc) {
+    return Set{reinterpret_cast<float*>(w + olse), reinterpret_cast<float*>(w + othr),
+               reinterpret_cast<float*>(w + ocz),  reinterpret_cast<float*>(w + oZ),
+               reinterpret_cast<int*>(w + ocnt),   reinterpret_cast<int*>(w + ocv),
+               reinterpret_cast<int*>(w + olive),  reinterpret_cast<int*>(w + olc)};
+  };
+  sets[0] = set_at(tp.off_lse, tp.off_thr, tp.off_cnt, tp.off_cv, tp.off_cz, tp.off_Z, tp.off_live, tp.off_live_cnt);
+  const bool overlap = keep && N > tp.chunk && ws_bytes >= tp.total_overlap;
+  SideStream* side = nullptr;
+  if (overlap) {
+    sets[1] = set_at(tp.alt_lse, tp.alt_thr, tp.alt_cnt, tp.alt_cv, tp.alt_cz, tp.alt_Z, tp.alt_live,
+                     tp.alt_live_cnt);
+    if ((st = side_stream(di->id, &side))) return st;
+    std::lock_guard<std::mutex> lk(g_setup_mu);
+    static bool carve[64] = {};
+    if (!carve[di->id]) {
+      cudaError_t ce = cudaFuncSetAttribute(topk_collect_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                            cudaSharedmemCarveoutMaxShared);
+      if (ce == cudaSuccess)
+        ce = cudaFuncSetAttribute(topk_select_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared);
+      if (ce != cudaSuccess) {
+        set_error("cudaFuncSetAttribute(top-K side kernels)", ce);
+        return FCKL_ERR_CUDA;
+      }
+      carve[di->id] = true;
+    }
+  }
   const int kbl = static_cast<int>(cdiv(d, ke));
-  for (int64_t r0 = 0; r0 < N; r0 += tp.chunk) {
+  // One chunk: pass 1 and the threshold on the caller's stream; pass 2 and the selection
+  // there too, or on the side stream.
+  auto topk_chunk = [&](int64_t r0, const Set& B, SideStream* side, int c) -> int {
+    int st = FCKL_OK;
+    float* lse = B.lse;
+    float* thr = B.thr;
+    int* cnt = B.cnt;
+    int* cv = B.cv;
+    float* cz = B.cz;
     const int rows = static_cast<int>(std::min<int64_t>(tp.chunk, N - r0));
     const void* Hc = static_cast<const uint8_t*>(Ht) + static_cast<size_t>(r0) * d * esz;
     if (f32) {
@@ -1187,7 +1262,7 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
     p.pl = pl;
     p.pc = reinterpret_cast<float*>(w + tp.off_pc);
     p.ld_part = tp.rows_alloc;
-    float* Z = reinterpret_cast<float*>(w + tp.off_Z);
+    float* Z = B.Z;
     if (keep) {  // pass 1 also stores the logits for the collect step
       if ((st = make_map(&p.tmC, Z, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, V, rows, uint64_t(tp.ldz) * 4, 32, 32)))
         return st;
@@ -1207,21 +1282,38 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
     const int tR = tp.thr_rows, tstride = tp.thr_stride;
     const int tblocks = static_cast<int>(cdiv(rows, tR));
     const size_t tsmem = static_cast<size_t>(tR) * tstride * 4;
-    int* live = keep ? reinterpret_cast<int*>(w + tp.off_live) : nullptr;
-    int* live_cnt = keep ? reinterpret_cast<int*>(w + tp.off_live_cnt) : nullptr;
+    int* live = keep ? B.live : nullptr;
+    int* live_cnt = keep ? B.live_cnt : nullptr;
     if ((st = launch(KIND_TOPK_THRESHOLD, s, "topk_threshold", [&] {
            topk_threshold_kernel<<<tblocks, 256, tsmem, s>>>(pm, pl, ld, tiles, rows, tR, tstride, K, lse, thr,
                                                              cnt, live, live_cnt);
          })))
       return st;
     // pass 2: every logit at or above the threshold becomes a candidate (logits kept from
-    // pass 1, or recomputed)
+    // pass 1, or recomputed), then the selection. With a side stream both run there, released
+    // together with the next chunk's pass 1 (one block per SM beside its CTAs), and the buffer
+    // set's join event is recorded after them.
     const int cmax = tp.cmax;
+    cudaStream_t ps = s;
+    if (side) {
+      cudaError_t e = cudaEventRecord(side->fork, s);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(side->s, side->fork, 0);
+      if (e != cudaSuccess) {
+        set_error("fork to the side stream", e);
+        return FCKL_ERR_CUDA;
+      }
+      ps = side->s;
+    }
     if (keep) {
-      const int grid = std::max(1, std::min(rows, di->sms * 8));
+      const int grid = std::max(1, std::min(rows, di->sms * (side ? 1 : 8)));
       const int64_t ldz = tp.ldz;
-      st = launch(KIND_TOPK_COLLECT_KEPT, s, "topk_collect_from_logits", [&] {
-        topk_collect_kernel<<<grid, 256, 0, s>>>(Z, ldz, rows, V, tiles, thr, live, live_cnt, cnt, cv, cz, cmax);
+      st = launch(KIND_TOPK_COLLECT_KEPT, ps, "topk_collect_from_logits", [&] {
+        if (side)
+          topk_collect_kernel<true><<<grid, 256, 0, ps>>>(Z, ldz, rows, V, tiles, thr, live, live_cnt, cnt, cv, cz,
+                                                          cmax);
+        else
+          topk_collect_kernel<false><<<grid, 256, 0, ps>>>(Z, ldz, rows, V, tiles, thr, live, live_cnt, cnt, cv,
+                                                           cz, cmax);
       });
     } else {
       p.thr = thr;
@@ -1233,15 +1325,40 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
                                                                              "topk_collect")
                : launch_tc<VOCAB_TILE, false, false, EPI_TOPK_COLLECT>(KIND_TOPK_COLLECT, di, p, s, "topk_collect");
     }
-    if (st) return st;
-    int32_t* io = idx + r0 * K;
-    float* lo = logp + r0 * K;
-    if ((st = launch(KIND_TOPK_SELECT, s, "topk_select", [&] {
-           topk_select_kernel<<<wblocks, 128, 0, s>>>(cv, cz, cnt, cmax, rows, K, lse, io, lo, status);
-         })))
-      return st;
+    if (!st) {
+      int32_t* io = idx + r0 * K;
+      float* lo = logp + r0 * K;
+      st = launch(KIND_TOPK_SELECT, ps, "topk_select", [&] {
+        if (side)
+          topk_select_kernel<true><<<wblocks, 128, 0, ps>>>(cv, cz, cnt, cmax, rows, K, lse, io, lo, status);
+        else
+          topk_select_kernel<false><<<wblocks, 128, 0, ps>>>(cv, cz, cnt, cmax, rows, K, lse, io, lo, status);
+      });
+    }
+    if (side) {  // recorded whatever failed: the caller's stream waits for it before returning
+      const cudaError_t e = cudaEventRecord(side->join_set[c & 1], side->s);
+      if (e != cudaSuccess && !st) {
+        set_error("join from the side stream", e);
+        st = FCKL_ERR_CUDA;
+      }
+    }
+    return st;
+  };
+  int c = 0;
+  for (int64_t r0 = 0; r0 < N; r0 += tp.chunk, ++c) {
+    const Set& B = sets[overlap ? (c & 1) : 0];
+    // the side work of chunk c-2 (same buffer set) is done before pass 1 overwrites its logits
+    if (overlap && c >= 2 && (st = wait_event(s, side->join_set[c & 1]))) break;
+    if ((st = topk_chunk(r0, B, overlap ? side : nullptr, c))) break;
   }
-  return FCKL_OK;
+  if (overlap) {  // nothing of this call stays outside the caller's stream order, error or not
+    // (an event not recorded by this call is already complete, or orders after earlier work)
+    for (cudaEvent_t ev : side->join_set) {
+      const int sj = wait_event(s, ev);
+      if (!st) st = sj;
+    }
+  }
+  return st;
 }
 
 int fckl_check(void* ws, void* stream) {

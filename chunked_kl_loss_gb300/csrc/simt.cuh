@@ -243,6 +243,10 @@ __global__ void __launch_bounds__(256) topk_threshold_kernel(const float* __rest
 // position and blocks stride over positions.
 constexpr int KC_BATCH = 4;
 
+// BESIDE = true: the same code as a separate function, launched beside a tensor-core product
+// with the largest shared-memory carve-out (as logit_grad_kernel<true>); it holds no shared
+// memory, so one block fits beside a product CTA.
+template <bool BESIDE>
 __global__ void __launch_bounds__(256) topk_collect_kernel(
     const float* __restrict__ Z, int64_t ld, int rows, int V, int tiles, const float* __restrict__ thr,
     const int* __restrict__ live, const int* __restrict__ live_cnt, int* __restrict__ cnt,
@@ -301,6 +305,8 @@ __global__ void __launch_bounds__(256) topk_collect_kernel(
 // (logit descending, token id ascending) and writes the first K as (id, logit - lse).
 // A row with more candidates than the buffer holds raises ST_CAPACITY (its output is then
 // not the exact top-K).
+// BESIDE: as for topk_collect_kernel (no shared memory either).
+template <bool BESIDE>
 __global__ void __launch_bounds__(128) topk_select_kernel(const int* __restrict__ cand_v,
                                                           const float* __restrict__ cand_z,
                                                           const int* __restrict__ cnt, int cmax, int rows, int K,

@@ -208,12 +208,17 @@ int fckl_forward_static(const void* H, const void* W, int dtype,
  * logit reaches); the second keeps the logits at or above the threshold as candidates, which
  * are then ranked exactly. The second pass reads the chunk's logits as the first pass stored
  * them when ws_bytes >= fckl_topk_kept_logits_workspace_bytes() (4 * chunk * V bytes more),
- * else it projects the chunk again; the outputs are the same either way. A row with more
+ * else it projects the chunk again; the outputs are the same either way. With ws_bytes >=
+ * fckl_topk_overlap_workspace_bytes() (a second set of one chunk's kept logits, candidates and
+ * per-row values) and N > chunk, each chunk's second pass and ranking run on the library's
+ * second stream (as in fckl_forward_backward) beside the next chunk's first pass, joined back
+ * into `stream` before the call returns; the outputs are again the same. A row with more
  * candidates than the buffer holds (min(V, 2048) slots, or V when K exceeds ceil(V/256)) is
  * reported as FCKL_ERR_CAPACITY by fckl_check. The workspace is at least
  * fckl_topk_workspace_bytes. V up to 1,310,720 (FCKL_ERR_UNSUPPORTED above). */
 size_t fckl_topk_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
 size_t fckl_topk_kept_logits_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
+size_t fckl_topk_overlap_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
 int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype,
                       int64_t N, int d, int V, int K, int chunk,
                       int32_t* idx, float* logp,

@@ -84,6 +84,20 @@ def test_workspace_size_rules(fckl):
     assert ov(2048, 256, 4096, 16, 4096, fckl.BF16) == ws(2048, 256, 4096, 16, 4096, fckl.BF16)
     assert ov(2049, 256, 4096, 16, 2048, fckl.BF16) > ws(2049, 256, 4096, 16, 2048, fckl.BF16)
     assert ov(0, 256, 4096, 16, 16, fckl.BF16) == 0 and ov(64, 250, 4096, 16, 16, fckl.BF16) == 0
+    # the top-K builder's overlap workspace: a second set of lse, threshold, count (rows x 4 B
+    # each), candidate ids and logits (rows x cmax x 4 B each), kept logits and live-tile lists
+    # and their lengths, after the kept-logits workspace (1 KiB rounding each), when N > chunk
+    for N, d, V, K, chunk in [(32768, 3072, 128256, 100, 2048), (130, 320, 2057, 100, 40)]:
+        rows = -(-min(chunk, N) // 256) * 256
+        tiles = -(-V // 256)
+        cmax = V if K > tiles else min(V, 2048)
+        want = 3 * rows * 4 + 2 * rows * cmax * 4 + rows * (-(-V // 8) * 8) * 4 + rows * tiles * 4 + rows * 4
+        extra = (lib.fckl_topk_overlap_workspace_bytes(N, d, V, K, chunk, fckl.BF16)
+                 - lib.fckl_topk_kept_logits_workspace_bytes(N, d, V, K, chunk, fckl.BF16))
+        assert 0 <= extra - want < 8 * 1024, (extra, want)
+    assert (lib.fckl_topk_overlap_workspace_bytes(100, 64, 1000, 8, 100, fckl.BF16)
+            == lib.fckl_topk_kept_logits_workspace_bytes(100, 64, 1000, 8, 100, fckl.BF16) > 0)
+    assert lib.fckl_topk_overlap_workspace_bytes(0, 64, 1000, 8, 100, fckl.BF16) == 0
     # outside the limits: 0
     assert ws(0, 256, 4096, 16, 16, fckl.BF16) == 0
     assert ws(64, 250, 4096, 16, 16, fckl.BF16) == 0  # d % 8 != 0

@@ -198,3 +198,44 @@ def test_topk_zero_logits(fckl):
     idx, logp = (t.cpu().numpy() for t in out[True])
     assert np.array_equal(idx, np.tile(np.arange(K, dtype=np.int32), (N, 1)))
     assert np.abs(logp + np.log(V)).max() <= 1e-5
+
+
+@pytest.mark.parametrize("N,d,V,K,chunk,dtype", [
+    (300, 256, 5000, 40, 128, "bf16"),   # 3 chunks, the last ragged
+    (64, 128, 1000, 20, 16, "bf16"),     # every token a candidate; 4 chunks of 16
+    (130, 320, 2057, 100, 40, "bf16"),   # V % 8 == 1; 4 chunks, the last 10 rows
+    (200, 128, 3000, 50, 64, "f32"),     # fp32 inputs (tf32 passes)
+    (100, 64, 1000, 8, 100, "bf16"),     # one chunk: no second set, the same workspace
+])
+def test_topk_overlap_is_bitwise_the_sequential_build(fckl, N, d, V, K, chunk, dtype):
+    """With the overlap workspace each chunk's collect and select run on the second stream
+    beside the next chunk's pass 1 (buffer sets alternating by chunk): the cache is bitwise the
+    one of the kept-logits workspace, and every chunk ran each step once."""
+    rng = np.random.default_rng(N + 3 * V)
+    Ht = synthetic.round_bf16(rng.standard_normal((N, d), dtype=np.float32))
+    Wt = synthetic.round_bf16(rng.standard_normal((V, d), dtype=np.float32) * 3.0 / np.sqrt(d))
+    dev = torch.device("cuda")
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    H = torch.from_numpy(Ht).to(dev).to(tdt)
+    W = torch.from_numpy(Wt).to(dev).to(tdt)
+    code = fckl.BF16 if dtype == "bf16" else fckl.F32
+    out, nbytes = {}, {}
+    for kind in ("topk", "topk_overlap"):
+        ws = fckl.Workspace(N, d, V, K, chunk, code, kind=kind)
+        fckl.profile_enable(True)
+        fckl.profile_read()
+        out[kind] = [t.clone() for t in fckl.teacher_topk(H, W, K, chunk, ws=ws)]
+        torch.cuda.synchronize()
+        prof = fckl.profile_read()
+        fckl.profile_enable(False)
+        assert fckl.check(ws) == fckl.OK
+        nbytes[kind] = ws.nbytes
+        chunks = -(-N // chunk)
+        for k in ("topk_logits_keep", "topk_threshold", "topk_collect_from_logits", "topk_select"):
+            assert prof[k][1] == chunks, (kind, k)
+    assert torch.equal(out["topk"][0], out["topk_overlap"][0])
+    assert torch.equal(out["topk"][1], out["topk_overlap"][1])
+    assert (nbytes["topk_overlap"] > nbytes["topk"]) == (N > chunk)
+    if dtype == "bf16":
+        idx, logp = (t.cpu().numpy() for t in out["topk_overlap"])
+        assert_topk_parity(idx.astype(np.int64), logp.astype(np.float64), Ht, Wt, K)
