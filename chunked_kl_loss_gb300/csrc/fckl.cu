@@ -49,6 +49,9 @@ enum Kind {
   KIND_BWD_GRAD_KEPT,
   KIND_TOPK_LOGITS_KEEP,
   KIND_TOPK_COLLECT_KEPT,
+  KIND_BWD_GRAD_KEPT_SIDE,      // the instances launched on the second stream beside a product
+  KIND_TOPK_COLLECT_KEPT_SIDE,
+  KIND_TOPK_SELECT_SIDE,
   KIND_COUNT
 };
 const char* const kKindNames[KIND_COUNT] = {"preprocess",     "fwd_logits_lse", "fwd_combine",
@@ -57,7 +60,9 @@ const char* const kKindNames[KIND_COUNT] = {"preprocess",     "fwd_logits_lse", 
                                             "wait_timeout_selftest", "topk_logits_stats", "topk_threshold",
                                             "topk_collect",           "topk_select",
                                             "fwd_logits_keep",        "bwd_grad_from_logits",
-                                            "topk_logits_keep",       "topk_collect_from_logits"};
+                                            "topk_logits_keep",       "topk_collect_from_logits",
+                                            "bwd_grad_from_logits_side", "topk_collect_from_logits_side",
+                                            "topk_select_side"};
 
 // ------------------------------------------------------------------ process state
 std::mutex g_mu;
@@ -708,7 +713,7 @@ int grad_from_kept(Run& r, int set, int64_t r0, int rows, cudaStream_t s, bool b
       done[r.di->id] = true;
     }
   }
-  return launch(KIND_BWD_GRAD_KEPT, s, "bwd_grad_from_logits", [&] {
+  return launch(beside ? KIND_BWD_GRAD_KEPT_SIDE : KIND_BWD_GRAD_KEPT, s, "bwd_grad_from_logits", [&] {
     if (beside)
       logit_grad_kernel<true><<<grid, GRAD_THREADS, 0, s>>>(G, ld, rows, V, K, sidx, spp, S, lse, wr, gsc, pm, ldp);
     else
@@ -855,6 +860,22 @@ int side_stream(int dev, SideStream** out) {
   }
   *out = &x;
   return FCKL_OK;
+}
+
+// Whether overlapping a chunk's side work with the next chunk's tensor-core pass pays. The side
+// kernels run one block per SM beside the product, so they take longer than alone; the product
+// must be long enough to cover them and the per-chunk fork and join. Measured on the one call
+// (V = 128256, chunk 2048): d = 3072 and 2048 gain 1-1.5%, d = 1536 and 2560 are even, d = 1024
+// loses 5%; at V = 32000, d = 2048 loses 2% and d = 1024 10%. Rule: a chunk's projection of at
+// least 5e11 FLOPs and, where the side pass scales with V like the projection (the G pass), d of
+// at least 2048. FCKL_OVERLAP (environment) forces it on (1) or off (0) when the workspace allows.
+bool overlap_pays(int64_t rows, int d, int V, bool side_scales_with_v) {
+  if (const char* env = std::getenv("FCKL_OVERLAP")) {
+    if (env[0] == '0' && env[1] == '\0') return false;
+    if (env[0] == '1' && env[1] == '\0') return true;
+  }
+  const double flops = 2.0 * double(rows) * double(d) * double(V);
+  return flops >= 5e11 && (!side_scales_with_v || d >= 2048);
 }
 
 // Makes stream s wait for event ev (stream order only, no host wait).
@@ -1084,7 +1105,8 @@ int fckl_forward_backward(const void* H, const void* W, int dtype, const int32_t
   r.dH = dH;
   r.dW = dW;
   // With the second buffer set in the workspace, G of each chunk overlaps the next forward.
-  const bool overlap = N > r.pl.chunk && ws_bytes >= r.pl.total_overlap;
+  const bool overlap =
+      N > r.pl.chunk && ws_bytes >= r.pl.total_overlap && overlap_pays(r.pl.chunk, d, V, true);
   SideStream* side = nullptr;
   if (overlap) {
     r.pl1 = second_set(r.pl);
@@ -1204,7 +1226,8 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
                reinterpret_cast<int*>(w + olive),  reinterpret_cast<int*>(w + olc)};
   };
   sets[0] = set_at(tp.off_lse, tp.off_thr, tp.off_cnt, tp.off_cv, tp.off_cz, tp.off_Z, tp.off_live, tp.off_live_cnt);
-  const bool overlap = keep && N > tp.chunk && ws_bytes >= tp.total_overlap;
+  const bool overlap =
+      keep && N > tp.chunk && ws_bytes >= tp.total_overlap && overlap_pays(tp.chunk, d, V, false);
   SideStream* side = nullptr;
   if (overlap) {
     sets[1] = set_at(tp.alt_lse, tp.alt_thr, tp.alt_cnt, tp.alt_cv, tp.alt_cz, tp.alt_Z, tp.alt_live,
@@ -1307,7 +1330,7 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
     if (keep) {
       const int grid = std::max(1, std::min(rows, di->sms * (side ? 1 : 8)));
       const int64_t ldz = tp.ldz;
-      st = launch(KIND_TOPK_COLLECT_KEPT, ps, "topk_collect_from_logits", [&] {
+      st = launch(side ? KIND_TOPK_COLLECT_KEPT_SIDE : KIND_TOPK_COLLECT_KEPT, ps, "topk_collect_from_logits", [&] {
         if (side)
           topk_collect_kernel<true><<<grid, 256, 0, ps>>>(Z, ldz, rows, V, tiles, thr, live, live_cnt, cnt, cv, cz,
                                                           cmax);
@@ -1328,7 +1351,7 @@ int fckl_teacher_topk(const void* Ht, const void* Wt, int dtype, int64_t N, int 
     if (!st) {
       int32_t* io = idx + r0 * K;
       float* lo = logp + r0 * K;
-      st = launch(KIND_TOPK_SELECT, ps, "topk_select", [&] {
+      st = launch(side ? KIND_TOPK_SELECT_SIDE : KIND_TOPK_SELECT, ps, "topk_select", [&] {
         if (side)
           topk_select_kernel<true><<<wblocks, 128, 0, ps>>>(cv, cz, cnt, cmax, rows, K, lse, io, lo, status);
         else

@@ -94,8 +94,12 @@ size_t fckl_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype
  * statistics) to fckl_workspace_bytes(); each chunk's G is then formed on a library-owned
  * second stream while the next chunk's forward runs on the caller's stream, and the caller's
  * stream waits for it before that chunk's gradient products, so the call still completes in
- * the caller's stream order and its results are bitwise those of the smaller workspace. With
- * N <= chunk it equals fckl_workspace_bytes(). 0 if the shape is outside the limits. */
+ * the caller's stream order and its results are bitwise those of the smaller workspace. The
+ * library overlaps only where it pays: a projection of at least 5e11 FLOPs per chunk
+ * (2 * chunk * d * V) and d >= 2048 (below that the G pass, at one block per SM beside the
+ * forward, outlasts it); otherwise the chunks run in sequence. The environment variable
+ * FCKL_OVERLAP=1 or 0 forces the choice. With N <= chunk it equals fckl_workspace_bytes().
+ * 0 if the shape is outside the limits. */
 size_t fckl_overlap_workspace_bytes(int64_t N, int d, int V, int K, int chunk, int dtype);
 
 /* Forward pass ("Hugging Face：让知识蒸馏廉价到可大规模运行", paragraph "Fused, chunked KL
@@ -212,7 +216,8 @@ int fckl_forward_static(const void* H, const void* W, int dtype,
  * fckl_topk_overlap_workspace_bytes() (a second set of one chunk's kept logits, candidates and
  * per-row values) and N > chunk, each chunk's second pass and ranking run on the library's
  * second stream (as in fckl_forward_backward) beside the next chunk's first pass, joined back
- * into `stream` before the call returns; the outputs are again the same. A row with more
+ * into `stream` before the call returns, when the first pass is at least 5e11 FLOPs per chunk
+ * (FCKL_OVERLAP=1 or 0 forces the choice); the outputs are again the same. A row with more
  * candidates than the buffer holds (min(V, 2048) slots, or V when K exceeds ceil(V/256)) is
  * reported as FCKL_ERR_CAPACITY by fckl_check. The workspace is at least
  * fckl_topk_workspace_bytes. V up to 1,310,720 (FCKL_ERR_UNSUPPORTED above). */

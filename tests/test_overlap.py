@@ -5,7 +5,10 @@ Every kernel computes what it does in the sequential order from the same inputs,
 outputs must be bitwise those of the minimum workspace (chunks one after another), which the
 other parity tests pin to the oracle; one case is also compared with the oracle directly. The
 profile counters show that the second buffer set was used (the G pass ran once per chunk, one
-block per SM beside the next forward for all but the last chunk).
+block per SM beside the next forward for all but the last chunk: the side instance's counter).
+The library overlaps only where it pays (a long enough projection per chunk, d >= 2048); the
+small shapes here force it with FCKL_OVERLAP=1, and test_overlap_rule checks the automatic
+choice.
 """
 import numpy as np
 import pytest
@@ -15,6 +18,11 @@ import synthetic
 from oracle import fckl_oracle as orc
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def forced_overlap(monkeypatch):
+    monkeypatch.setenv("FCKL_OVERLAP", "1")
 
 
 def to_dev(x, dtype):
@@ -67,7 +75,8 @@ def test_overlap_is_bitwise_the_sequential_one_call(fckl, N, d, V, K, chunk, dty
         assert a.dtype == b.dtype and a.shape == b.shape
         assert torch.equal(a, b)
     chunks = -(-N // chunk)
-    assert p_seq["bwd_grad_from_logits"][1] == chunks and p_ovl["bwd_grad_from_logits"][1] == chunks
+    assert p_seq["bwd_grad_from_logits"][1] == chunks and p_seq["bwd_grad_from_logits_side"][1] == 0
+    assert p_ovl["bwd_grad_from_logits"][1] == 1 and p_ovl["bwd_grad_from_logits_side"][1] == chunks - 1
     assert p_ovl["fwd_logits_keep"][1] == chunks and p_ovl["bwd_dW_gemm"][1] == chunks
     if chunks > 1:
         assert n_ovl > n_seq
@@ -115,3 +124,26 @@ def test_overlap_captured_in_a_cuda_graph(fckl):
         assert fckl.check(ws) == fckl.OK
         for u, v in zip((loss, lse, dH, dW), ref):
             assert torch.equal(u, v)
+
+
+def test_overlap_rule(fckl, monkeypatch):
+    """Without FCKL_OVERLAP the library overlaps only where it pays: at d = 3072, V = 128256,
+    chunk 2048 (a 1.6e12-FLOP projection per chunk) the G pass of the first chunk runs beside
+    the second chunk's forward; at d = 256 it does not, even with the overlap workspace; and
+    FCKL_OVERLAP=0 turns it off. The outputs are the same bits in every case."""
+    res = {}
+    for name, (N, d, V, K, chunk), env in (("big", (4096, 3072, 128256, 100, 2048), None),
+                                           ("big_off", (4096, 3072, 128256, 100, 2048), "0"),
+                                           ("small", (600, 256, 5000, 40, 128), None)):
+        if env is None:
+            monkeypatch.delenv("FCKL_OVERLAP", raising=False)
+        else:
+            monkeypatch.setenv("FCKL_OVERLAP", env)
+        x = synthetic.make_inputs(N, d, V, K, dtype="bf16", seed=9)
+        out, prof, _ = one_call(fckl, to_dev(x, "bf16"), chunk, "loss_overlap", fckl.BF16)
+        res[name] = (out, prof)
+    assert res["big"][1]["bwd_grad_from_logits_side"][1] == 1
+    assert res["big_off"][1]["bwd_grad_from_logits_side"][1] == 0
+    assert res["small"][1]["bwd_grad_from_logits_side"][1] == 0
+    for a, b in zip(res["big"][0], res["big_off"][0]):
+        assert torch.equal(a, b)

@@ -207,10 +207,12 @@ def test_topk_zero_logits(fckl):
     (200, 128, 3000, 50, 64, "f32"),     # fp32 inputs (tf32 passes)
     (100, 64, 1000, 8, 100, "bf16"),     # one chunk: no second set, the same workspace
 ])
-def test_topk_overlap_is_bitwise_the_sequential_build(fckl, N, d, V, K, chunk, dtype):
+def test_topk_overlap_is_bitwise_the_sequential_build(fckl, N, d, V, K, chunk, dtype, monkeypatch):
     """With the overlap workspace each chunk's collect and select run on the second stream
-    beside the next chunk's pass 1 (buffer sets alternating by chunk): the cache is bitwise the
-    one of the kept-logits workspace, and every chunk ran each step once."""
+    beside the next chunk's pass 1 (buffer sets alternating by chunk; forced with FCKL_OVERLAP=1,
+    since these projections are too short for the library to choose it): the cache is bitwise
+    the one of the kept-logits workspace, and every chunk ran each step once."""
+    monkeypatch.setenv("FCKL_OVERLAP", "1")
     rng = np.random.default_rng(N + 3 * V)
     Ht = synthetic.round_bf16(rng.standard_normal((N, d), dtype=np.float32))
     Wt = synthetic.round_bf16(rng.standard_normal((V, d), dtype=np.float32) * 3.0 / np.sqrt(d))
@@ -231,8 +233,12 @@ def test_topk_overlap_is_bitwise_the_sequential_build(fckl, N, d, V, K, chunk, d
         assert fckl.check(ws) == fckl.OK
         nbytes[kind] = ws.nbytes
         chunks = -(-N // chunk)
-        for k in ("topk_logits_keep", "topk_threshold", "topk_collect_from_logits", "topk_select"):
+        for k in ("topk_logits_keep", "topk_threshold"):
             assert prof[k][1] == chunks, (kind, k)
+        side = kind == "topk_overlap" and N > chunk
+        for k in ("topk_collect_from_logits", "topk_select"):
+            assert prof[k][1] == (0 if side else chunks), (kind, k)
+            assert prof[k + "_side"][1] == (chunks if side else 0), (kind, k)
     assert torch.equal(out["topk"][0], out["topk_overlap"][0])
     assert torch.equal(out["topk"][1], out["topk_overlap"][1])
     assert (nbytes["topk_overlap"] > nbytes["topk"]) == (N > chunk)
