@@ -361,7 +361,15 @@ def kernel_work(w, kname):
     return flops, byts
 
 
-def path_summary(w, api, t_ms, steps, world, prof, peak_sus, peak_src, hbm_peak=None):
+def peak_clock_mhz(peaks):
+    """Median SM clock under load while the sustained peak was measured, or None."""
+    c = peaks.get("clocks_under_load") if isinstance(peaks, dict) else None
+    v = c.get("sm_mhz_median") if isinstance(c, dict) else None
+    return float(v) if isinstance(v, (int, float)) and v > 0 else None
+
+
+def path_summary(w, api, t_ms, steps, world, prof, peak_sus, peak_src, hbm_peak=None, run_mhz=None,
+                 peak_mhz=None):
     """Throughput of one timed path and the roofline of its dominant kernel.
 
     tflops_8NdV is the metric's count (8 N d V FLOPs per step: the four products of the
@@ -395,6 +403,11 @@ def path_summary(w, api, t_ms, steps, world, prof, peak_sus, peak_src, hbm_peak=
                                 else f"{peak_src} HBM copy bandwidth"),
                 "flops_per_launch": flops_per_launch, "algorithmic_bytes_per_launch": bytes_per_launch,
                 "tensor_frac": k_tfl / peak_sus, "hbm_frac": k_gbs / hbm, "avg_launch_ms": kms / kn}
+        if tensor_bound and run_mhz and peak_mhz:
+            # context for box-to-box differences under the power cap: the same fraction at the
+            # clock the sustained peak was measured at (frac itself is the measured one)
+            roof.update({"run_sm_mhz": run_mhz, "peak_sm_mhz": peak_mhz,
+                         "frac_at_peak_clock": k_tfl / peak_sus * peak_mhz / run_mhz})
     total = max(1e-9, sum(u[0] for u in prof.values()))
     return {"value": world * w.N * steps / (t_ms / 1e3), "ms_per_step": ms_step,
             "tflops_8NdV": tfl,
@@ -568,7 +581,9 @@ def run_ours(args):
     peaks, peak_src = measured_peaks()
     peak_sus = peak_value(peaks, "bf16_tflops_sustained")
     hbm_peak = peak_value(peaks, "hbm_gbs")
-    head = path_summary(w, args.api, t_max, args.steps, world, prof, peak_sus, peak_src, hbm_peak)
+    pk_mhz = peak_clock_mhz(peaks)
+    head = path_summary(w, args.api, t_max, args.steps, world, prof, peak_sus, peak_src, hbm_peak,
+                        (clk or {}).get("sm_mhz"), pk_mhz)
     line = {
         "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
@@ -588,7 +603,8 @@ def run_ours(args):
     }
     if other is not None:
         o_api, o_ms, o_launch, o_prof, o_clk = other
-        o = path_summary(w, o_api, o_ms, args.steps, world, o_prof, peak_sus, peak_src, hbm_peak)
+        o = path_summary(w, o_api, o_ms, args.steps, world, o_prof, peak_sus, peak_src, hbm_peak,
+                         (o_clk or {}).get("sm_mhz"), pk_mhz)
         o.update({"api": o_api, "logits": config_of(w, o_api)["logits"], "gpu_launches": o_launch,
                   "clocks": o_clk, "steps": args.steps, "warmup": args.warmup})
         line[o_api] = o

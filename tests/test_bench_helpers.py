@@ -98,3 +98,11 @@ def test_path_summary_counts_and_kernel_roofline():
         assert abs(r["hbm_frac"] - b / chunks / 1e-3 / 1e9 / 6700.0) < 1e-9
         sep = bench.path_summary(w, "separate", t_ms, steps, 1, prof, 1700.0, "measured", 6700.0)
         assert sep["tflops_executed"] == sep["tflops_8NdV"]
+        # with the clocks: the tensor-bound fraction is also given at the peak's clock
+        c = bench.path_summary(w, "fused", t_ms, steps, 1, prof, 1700.0, "measured", 6700.0, 1450.0, 1507.0)
+        if bound == "tensor":
+            assert abs(c["roofline"]["frac_at_peak_clock"] - r["frac"] * 1507.0 / 1450.0) < 1e-12
+        else:
+            assert "frac_at_peak_clock" not in c["roofline"]
+    assert bench.peak_clock_mhz({"clocks_under_load": {"sm_mhz_median": 1507.0}}) == 1507.0
+    assert bench.peak_clock_mhz({}) is None
